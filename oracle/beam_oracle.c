@@ -1,0 +1,311 @@
+/*
+ * beam_oracle.c -- plain, slow CPU oracle for the Beam sublayer-boundary path.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline / reference leg may load this library.  It shares no code with the
+ * CUDA library (no headers, helpers or tables); the two meet only on the seeded inputs.
+ *
+ * Every function works one token at a time, in program order, in FP32 arithmetic with the BF16
+ * round-to-nearest-even points the pages state.  Two steps are deliberately more accurate than a
+ * GPU can afford, so the oracle is the exact side of every comparison:
+ *   - a row's sum of squares is accumulated in double and rounded once to FP32;
+ *   - exp / cos / sin / pow are evaluated in double and rounded once to FP32.
+ * Build with -ffp-contract=off: a contracted multiply-add would change the FP32 rounding steps.
+ *
+ * Pages cited (titles as printed):
+ *   [vLLM]  "Serving Reflection Beam auf vLLM ab Tag 0"
+ *   [SGL]   "SGLang 支撑编程模型 Beam 生产部署"
+ *
+ * Parity pins: every function here is pinned by the CPU tests (tests/test_oracle_*.py) against
+ * closed forms, invariants and library routines; none is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------------------------ */
+/* BF16                                                                                        */
+/* ------------------------------------------------------------------------------------------ */
+
+/* FP32 -> BF16 with IEEE round-to-nearest-even.  NaN stays NaN (quiet bit set); overflow past
+ * the largest finite BF16 goes to infinity; subnormals round like any other value.
+ * [SGL] "三明治归一化与深度缩放残差": both scaled residual operands are rounded to the
+ * activation type (BF16) before the add; RNE is the IEEE default rounding. */
+uint16_t orc_bf16_rne(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)          /* NaN: keep sign and payload top, force quiet */
+        return (uint16_t)((u >> 16) | 0x0040u);
+    uint32_t lsb = (u >> 16) & 1u;                /* ties go to the even neighbour */
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+float orc_bf16_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* value of x after a BF16 rounding, as FP32 */
+static float bf16_round(float x) { return orc_bf16_to_f32(orc_bf16_rne(x)); }
+
+void orc_bf16_rne_array(const float *in, uint16_t *out, int64_t count)
+{
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = orc_bf16_rne(in[i]);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* RMSNorm scale                                                                               */
+/* ------------------------------------------------------------------------------------------ */
+
+/* r = 1 / sqrt(mean_j v_j^2 + eps).
+ * Each square is an FP32 product; the squares are summed in double (for BF16 inputs every term
+ * is exact and the double sum is exact to ~1e-13 relative) and the sum is rounded once to FP32;
+ * the mean is that FP32 sum divided by the length in FP32; then FP32 add, IEEE sqrt, IEEE div.
+ * [vLLM] "MoE und Residual-Stream", bullet "Sandwich-Norm": an RMSNorm before and after every
+ * sublayer; [vLLM] "Agentengetriebene Optimierung", change 1: FP32 math. */
+static float rms_inv(const float *v, int32_t len, float eps)
+{
+    double acc = 0.0;
+    for (int32_t j = 0; j < len; ++j) {
+        float sq = v[j] * v[j];
+        acc += (double)sq;
+    }
+    float ms = (float)acc;
+    float mean = ms / (float)len;
+    return 1.0f / sqrtf(mean + eps);
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Sublayer boundary: post-RMSNorm -> depth-scaled residual add -> next pre-RMSNorm            */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Coefficients of the n-th residual add, h <- sqrt((n-1)/n) * h + x / sqrt(n), as FP32.
+ * [vLLM] "MoE und Residual-Stream", bullet "Tiefenskalierte Residuen". */
+void orc_residual_scales(int32_t n, float *alpha, float *s)
+{
+    *alpha = (float)sqrt((double)(n - 1) / (double)n);
+    *s = (float)sqrt((double)n);
+}
+
+/* One token of the boundary chain on an FP32 copy of the sublayer output xf[H].
+ *   a1  r  = rms_inv(x);            xhat_j = bf16((x_j * r) * wpost_j)
+ *   a2  a_j = bf16(alpha * h_j);    b_j = bf16(xhat_j / s);    h'_j = bf16(a_j + b_j)
+ *   a3  r' = rms_inv(h');           y_j = bf16((h'_j * r') * wpre_j)
+ * [vLLM] "Agentengetriebene Optimierung", change 1 (post-norm, scaled add and next pre-norm in
+ * one pass, FP32 math, the reference BF16 rounding points); [SGL] "三明治归一化与深度缩放残差"
+ * (both scaled operands rounded to BF16 before the add; the normalised branch result is a
+ * materialised BF16 tensor in the unfused path). */
+static void boundary_token(uint16_t *h_out, uint16_t *y_out, const uint16_t *h_in,
+                           const float *xf, const uint16_t *w_post, const uint16_t *w_pre,
+                           int32_t H, float alpha, float s, float eps, float *rstd2,
+                           float *work /* [2H] */)
+{
+    float *xhat = work;
+    float *hp = work + H;
+
+    float r1 = rms_inv(xf, H, eps);
+    for (int32_t j = 0; j < H; ++j) {
+        float t = xf[j] * r1;
+        xhat[j] = bf16_round(t * orc_bf16_to_f32(w_post[j]));
+    }
+    for (int32_t j = 0; j < H; ++j) {
+        float a = bf16_round(alpha * orc_bf16_to_f32(h_in[j]));
+        float b = bf16_round(xhat[j] / s);
+        hp[j] = bf16_round(a + b);
+    }
+    float r2 = rms_inv(hp, H, eps);
+    for (int32_t j = 0; j < H; ++j) {
+        float t = hp[j] * r2;
+        y_out[j] = orc_bf16_rne(t * orc_bf16_to_f32(w_pre[j]));
+        h_out[j] = orc_bf16_rne(hp[j]);
+    }
+    if (rstd2) {
+        rstd2[0] = r1;
+        rstd2[1] = r2;
+    }
+}
+
+/* h_in, x_in, h_out, y_out: [T, H] BF16 bit patterns, rows contiguous.  rstd_out: [T, 2] or NULL.
+ * work: caller scratch of 3*H floats.  Outputs must not alias inputs. */
+void orc_boundary(uint16_t *h_out, uint16_t *y_out, const uint16_t *h_in, const uint16_t *x_in,
+                  const uint16_t *w_post, const uint16_t *w_pre, int64_t T, int32_t H, int32_t n,
+                  float eps, float *rstd_out, float *work)
+{
+    float alpha, s;
+    orc_residual_scales(n, &alpha, &s);
+    float *xf = work + 2 * (int64_t)H;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int32_t j = 0; j < H; ++j)
+            xf[j] = orc_bf16_to_f32(x_in[t * H + j]);
+        boundary_token(h_out + t * H, y_out + t * H, h_in + t * H, xf, w_post, w_pre, H, alpha,
+                       s, eps, rstd_out ? rstd_out + 2 * t : 0, work);
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* MoE top-K combine fused ahead of the boundary                                               */
+/* ------------------------------------------------------------------------------------------ */
+
+/* x_j = bf16( sum_k c_k * e_{k,j} ),  c_k = fp32(w_k * routed_scaling).
+ * The sum runs in slot order k = 0..K-1, one FP32 fused multiply-add per slot, from +0.
+ * Then the boundary chain on x.
+ * [vLLM] "MoE und Residual-Stream", bullet "MoE im DeepSeek-V3-Stil" (top-8, renormalised
+ * weights scaled by 2.5); [vLLM] "Agentengetriebene Optimierung", change 3 (the boundary kernel
+ * also combines the top-8 expert outputs); [SGL] "稠密层与分组 MoE 路由" (FP32 routing
+ * coefficients, scaling factor applied in the combine); [SGL] kernel-fusion paragraph (local
+ * expert sum, routing scale and BF16 rounding fused).
+ * expert_out: [T, K, H]; topk_w: [T, K] FP32; x_out: [T, H] or NULL (the combined x, for tests). */
+void orc_moe_combine_boundary(uint16_t *h_out, uint16_t *y_out, const uint16_t *h_in,
+                              const uint16_t *expert_out, const float *topk_w,
+                              float routed_scaling, const uint16_t *w_post,
+                              const uint16_t *w_pre, int64_t T, int32_t H, int32_t K, int32_t n,
+                              float eps, float *rstd_out, uint16_t *x_out, float *work)
+{
+    float alpha, s;
+    orc_residual_scales(n, &alpha, &s);
+    float *xf = work + 2 * (int64_t)H;
+    float c[64];
+    for (int64_t t = 0; t < T; ++t) {
+        for (int32_t k = 0; k < K; ++k)
+            c[k] = topk_w[t * K + k] * routed_scaling;
+        const uint16_t *e = expert_out + t * (int64_t)K * H;
+        for (int32_t j = 0; j < H; ++j) {
+            float acc = 0.0f;
+            for (int32_t k = 0; k < K; ++k)
+                acc = fmaf(c[k], orc_bf16_to_f32(e[(int64_t)k * H + j]), acc);
+            xf[j] = bf16_round(acc);
+            if (x_out)
+                x_out[t * H + j] = orc_bf16_rne(acc);
+        }
+        boundary_token(h_out + t * H, y_out + t * H, h_in + t * H, xf, w_post, w_pre, H, alpha,
+                       s, eps, rstd_out ? rstd_out + 2 * t : 0, work);
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Per-head Q/K RMSNorm fused with RoPE (sliding-window layers) or SSMax (NoPE layers)          */
+/* ------------------------------------------------------------------------------------------ */
+
+/* qhat_d = (v_d * r) * w_d in FP32, no rounding, r = rms_inv over the head.
+ * [vLLM] "Attention", bullet "GQA mit Per-Head-Q/K-Norm": Q and K are RMS-normalised per head
+ * before RoPE or SSMax; [SGL] "混合注意力与输出门控". */
+static void head_norm(float *qhat, const uint16_t *v, const uint16_t *w, int32_t D, float eps,
+                      float *tmp)
+{
+    for (int32_t d = 0; d < D; ++d)
+        tmp[d] = orc_bf16_to_f32(v[d]);
+    float r = rms_inv(tmp, D, eps);
+    for (int32_t d = 0; d < D; ++d)
+        qhat[d] = (tmp[d] * r) * orc_bf16_to_f32(w[d]);
+}
+
+/* Rotary frequencies of the half-rotation convention: inv_freq_i = fp32(theta^(-2i/D)). */
+void orc_rope_inv_freq(float theta, int32_t D, float *inv_freq)
+{
+    for (int32_t i = 0; i < D / 2; ++i)
+        inv_freq[i] = (float)pow((double)theta, -2.0 * (double)i / (double)D);
+}
+
+/* In place on q rows [T, nq, D] (row stride q_stride elements) and k rows [T, nk, D].
+ * Per token: angle_i = fp32(fp32(pos) * inv_freq_i); c_i, s_i = cos, sin of that FP32 angle
+ * (double, rounded to FP32).  Per head, half rotation over the pairs (i, i + D/2):
+ *   out_i       = bf16( fp32(qhat_i * c_i) - fp32(qhat_{i+D/2} * s_i) )
+ *   out_{i+D/2} = bf16( fp32(qhat_{i+D/2} * c_i) + fp32(qhat_i * s_i) )
+ * [vLLM] "Attention", bullet "Hybride Sliding-Window- und NoPE-Schichten" (RoPE on the 43
+ * sliding-window layers); [SGL] kernel-fusion paragraph (Q/K norm fused with RoPE). */
+void orc_qk_norm_rope(uint16_t *q, uint16_t *k, int64_t q_stride, int64_t k_stride,
+                      const uint16_t *wq, const uint16_t *wk, const int64_t *pos, int64_t T,
+                      int32_t nq, int32_t nk, int32_t D, float eps, float theta, float *work)
+{
+    int32_t half = D / 2;
+    float *inv_freq = work;           /* [D/2] */
+    float *cs = work + half;          /* [D/2] */
+    float *sn = work + 2 * half;      /* [D/2] */
+    float *qhat = work + 3 * half;    /* [D] */
+    float *tmp = work + 3 * half + D; /* [D] */
+    orc_rope_inv_freq(theta, D, inv_freq);
+    for (int64_t t = 0; t < T; ++t) {
+        float p = (float)pos[t];
+        for (int32_t i = 0; i < half; ++i) {
+            float ang = p * inv_freq[i];
+            cs[i] = (float)cos((double)ang);
+            sn[i] = (float)sin((double)ang);
+        }
+        for (int32_t hd = 0; hd < nq + nk; ++hd) {
+            uint16_t *row = hd < nq ? q + t * q_stride + (int64_t)hd * D
+                                    : k + t * k_stride + (int64_t)(hd - nq) * D;
+            const uint16_t *w = hd < nq ? wq : wk;
+            head_norm(qhat, row, w, D, eps, tmp);
+            for (int32_t i = 0; i < half; ++i) {
+                float lo = qhat[i] * cs[i] - qhat[i + half] * sn[i];
+                float hi = qhat[i + half] * cs[i] + qhat[i] * sn[i];
+                row[i] = orc_bf16_rne(lo);
+                row[i + half] = orc_bf16_rne(hi);
+            }
+        }
+    }
+}
+
+/* SSMax query scale for a 0-based position: fp32((1 + (pos + 1) / base) ^ expo).
+ * [vLLM] "Attention", bullet "SSMax auf NoPE-Schichten": (1 + p/2048)^0.1 with p 1-based;
+ * [SGL] "稠密层与分组 MoE 路由", SSMax paragraph: the same with a 0-based p as (1+(p+1)/2048)^0.1. */
+float orc_ssmax_scale(int64_t pos, float base, float expo)
+{
+    double p1 = (double)pos + 1.0;
+    return (float)pow(1.0 + p1 / (double)base, (double)expo);
+}
+
+/* In place.  Q: out = bf16( ((q * r) * wq) * ssmax_scale(pos) );  K: out = bf16( (k * r) * wk ).
+ * The scale multiplies queries only, after their norm. */
+void orc_qk_norm_ssmax(uint16_t *q, uint16_t *k, int64_t q_stride, int64_t k_stride,
+                       const uint16_t *wq, const uint16_t *wk, const int64_t *pos, int64_t T,
+                       int32_t nq, int32_t nk, int32_t D, float eps, float base, float expo,
+                       float *work)
+{
+    float *qhat = work;
+    float *tmp = work + D;
+    for (int64_t t = 0; t < T; ++t) {
+        float sc = orc_ssmax_scale(pos[t], base, expo);
+        for (int32_t hd = 0; hd < nq + nk; ++hd) {
+            int is_q = hd < nq;
+            uint16_t *row = is_q ? q + t * q_stride + (int64_t)hd * D
+                                 : k + t * k_stride + (int64_t)(hd - nq) * D;
+            head_norm(qhat, row, is_q ? wq : wk, D, eps, tmp);
+            for (int32_t d = 0; d < D; ++d)
+                row[d] = orc_bf16_rne(is_q ? qhat[d] * sc : qhat[d]);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
+/* Sigmoid attention-output gate                                                               */
+/* ------------------------------------------------------------------------------------------ */
+
+/* out = bf16( attn * sigma ),  sigma = 1 / (1 + e),  e = fp32(exp(-z)),  z = fp32(gate + bias_h).
+ * FP32 steps; exp in double rounded to FP32.  bias: [n_heads] FP32.
+ * [vLLM] "Attention", bullet "Sigmoid-Output-Gate" (each head's output times sigma(gate + bias),
+ * per-head learned bias, a head can be switched off); [SGL] "混合注意力与输出门控" and the
+ * kernel-fusion paragraph (bias add, sigmoid and multiply in one kernel). */
+void orc_attn_gate(uint16_t *out, const uint16_t *attn, const uint16_t *gate, const float *bias,
+                   int64_t T, int32_t nh, int32_t D, int64_t attn_stride, int64_t gate_stride,
+                   int64_t out_stride)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        for (int32_t h = 0; h < nh; ++h) {
+            for (int32_t d = 0; d < D; ++d) {
+                int64_t c = (int64_t)h * D + d;
+                float z = orc_bf16_to_f32(gate[t * gate_stride + c]) + bias[h];
+                float e = (float)exp(-(double)z);
+                float sig = 1.0f / (1.0f + e);
+                float a = orc_bf16_to_f32(attn[t * attn_stride + c]);
+                out[t * out_stride + c] = orc_bf16_rne(a * sig);
+            }
+        }
+    }
+}
