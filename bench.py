@@ -1,0 +1,540 @@
+"""Benchmark of the Beam sublayer-boundary path on GB300.
+
+One step = one pass of every kernel of the path over an 8 x 2048 = 16384-token prefill batch
+(hidden 5120, 48 query / 8 KV heads of 128, top-8 experts), all inputs resident in HBM:
+    qk_norm_rope  ->  qk_norm_ssmax  ->  attn_gate  ->  boundary  ->  moe_combine_boundary
+Every kernel streams more than the 129 MB L2 per launch, so no input survives in L2 from one
+launch of it to the next.
+
+Prints one JSON line (rank 0): whole-job tokens/s, per-kernel time / HBM GB/s / roofline
+fraction, the roofline of the dominant kernel, the batch-1 decode chain (104 boundaries in one
+CUDA graph, us per boundary), an end-to-end number through host buffers, the CPU oracle as a
+baseline, and the SM clocks seen while the timed region ran.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun each rank runs its own replica on its own GPU (the path has no exchange step):
+the units are independent tokens, so N ranks process N batches ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import beam_inputs as bi  # noqa: E402
+
+METRIC = ("boundary tokens/s & HBM GB/s (% of GB300 peak) at T=16384; "
+          "µs/boundary at T=1")
+T_PREFILL = 16384
+H = bi.HIDDEN
+NQ, NKV, D, K = bi.N_Q_HEADS, bi.N_KV_HEADS, bi.HEAD_DIM, bi.TOP_K
+FALLBACK_HBM_GBS = 6800.0
+
+# Algorithmic HBM bytes per token of each kernel (reads + writes of the tensors it must touch).
+BYTES_PER_TOKEN = {
+    "qk_norm_rope": 2 * (NQ + NKV) * D * 2 + 8,       # Q, K read + written, position
+    "qk_norm_ssmax": 2 * (NQ + NKV) * D * 2 + 8,
+    "attn_gate": 3 * NQ * D * 2,                       # attn, gate read; out written
+    "boundary": 4 * H * 2,                             # x, h read; h', y written
+    "moe_combine_boundary": (K + 1) * H * 2 + 2 * H * 2 + K * 4,  # experts, h; h', y; weights
+}
+KERNELS = list(BYTES_PER_TOKEN)
+SOURCES = {
+    "qk_norm_rope": "attention.cu", "qk_norm_ssmax": "attention.cu", "attn_gate": "attention.cu",
+    "boundary": "boundary.cu", "moe_combine_boundary": "boundary.cu",
+}
+
+
+# ---------------------------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws: int, backend: str):
+    if ws > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(ws: int):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, max clock, throttle reasons) while the GPU is busy."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.rows = []
+        self.proc = None
+        self.ident = None
+        try:
+            uuid = torch.cuda.get_device_properties(device_index).uuid
+            self.ident = f"GPU-{uuid}"
+        except Exception:
+            self.ident = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.ident:
+            cmd += ["-i", self.ident]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except FileNotFoundError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 7:
+                self.rows.append((time.perf_counter(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = [r for t, r in self.rows if t0 - 0.15 <= t <= t1 + 0.15] or \
+            [r for _, r in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = sorted({self.REASONS[i] for r in rows for i in range(4)
+                          if r[3 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((num(r[2]) or 0.0) for r in rows)}
+
+
+# ---------------------------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------------------------
+
+def make_host_inputs(T: int, seed: int = 0) -> dict:
+    """Seeded synthetic inputs of one step, on the host (pinned when CUDA is available)."""
+    a_rope = bi.attn_qk_case(T=T, seed=seed, pos_mode="uniform")
+    a_ss = bi.attn_qk_case(T=T, seed=seed + 1, pos_mode="contiguous")
+    g = bi.gate_case(T=T, seed=seed + 2)
+    pb = bi.prefill_boundary_case(T=T, seed=seed + 3)
+    m = bi.moe_case(T=T, seed=seed + 4)
+    host = {
+        "q_r": a_rope["q"], "k_r": a_rope["k"], "pos_r": a_rope["pos"],
+        "wq_r": a_rope["wq"], "wk_r": a_rope["wk"],
+        "q_s": a_ss["q"], "k_s": a_ss["k"], "pos_s": a_ss["pos"],
+        "wq_s": a_ss["wq"], "wk_s": a_ss["wk"],
+        "attn": g["attn"], "gate": g["gate"], "bias": g["bias"],
+        "h": pb["h"], "x": pb["x"], "w_post": pb["w_post"], "w_pre": pb["w_pre"],
+        "h_m": m["h"], "e": m["e"], "topk_w": m["topk_w"],
+        "w_post_m": m["w_post"], "w_pre_m": m["w_pre"],
+    }
+    if torch.cuda.is_available():
+        host = {k: v.pin_memory() for k, v in host.items()}
+    return host
+
+
+INPUT_KEYS = ["q_r", "k_r", "pos_r", "q_s", "k_s", "pos_s", "attn", "gate", "bias", "h", "x",
+              "h_m", "e", "topk_w"]
+WEIGHT_KEYS = ["wq_r", "wk_r", "wq_s", "wk_s", "w_post", "w_pre", "w_post_m", "w_pre_m"]
+
+
+class Step:
+    """Device buffers of one step and the launch sequence through the C ABI."""
+
+    def __init__(self, host: dict, device):
+        import residual_stream_norm_gb300 as rsn
+        self.rsn = rsn
+        self.dev = {k: v.to(device, non_blocking=True) for k, v in host.items()}
+        T = host["h"].shape[0]
+        self.T = T
+        d = self.dev
+        self.out_gate = torch.empty_like(d["attn"])
+        self.y = torch.empty_like(d["h"])
+        self.y_m = torch.empty_like(d["h_m"])
+        self.layer = 0
+        self.lib = rsn.lib()
+
+    def n_pair(self, i: int) -> tuple[int, int]:
+        layer = i % 52
+        return 2 * layer + 1, 2 * layer + 2
+
+    def launch(self, i: int, events=None) -> int:
+        """Launch the five kernels of step i on the current stream; returns launches."""
+        d, L, st = self.dev, self.lib, torch.cuda.current_stream().cuda_stream
+        n_attn, n_ffn = self.n_pair(i)
+        wi = (n_attn - 1) % bi.N_BOUNDARIES
+        rec = events.__getitem__ if events is not None else None
+        calls = (
+            ("beam_qk_norm_rope_fwd", (d["q_r"].data_ptr(), d["k_r"].data_ptr(), NQ * D, NKV * D,
+                                        d["wq_r"].data_ptr(), d["wk_r"].data_ptr(),
+                                        d["pos_r"].data_ptr(), self.T, NQ, NKV, D, bi.EPS,
+                                        bi.ROPE_THETA, st)),
+            ("beam_qk_norm_ssmax_fwd", (d["q_s"].data_ptr(), d["k_s"].data_ptr(), NQ * D, NKV * D,
+                                         d["wq_s"].data_ptr(), d["wk_s"].data_ptr(),
+                                         d["pos_s"].data_ptr(), self.T, NQ, NKV, D, bi.EPS,
+                                         bi.SSMAX_BASE, bi.SSMAX_EXP, st)),
+            ("beam_attn_gate_fwd", (self.out_gate.data_ptr(), d["attn"].data_ptr(),
+                                     d["gate"].data_ptr(), d["bias"].data_ptr(), self.T, NQ, D,
+                                     NQ * D, NQ * D, NQ * D, st)),
+            ("beam_boundary_fwd", (d["h"].data_ptr(), self.y.data_ptr(), d["h"].data_ptr(),
+                                    d["x"].data_ptr(), d["w_post"][wi].data_ptr(),
+                                    d["w_pre"][wi].data_ptr(), self.T, H, n_attn, bi.EPS, None,
+                                    st)),
+            ("beam_moe_combine_boundary_fwd", (d["h_m"].data_ptr(), self.y_m.data_ptr(),
+                                                d["h_m"].data_ptr(), d["e"].data_ptr(),
+                                                d["topk_w"].data_ptr(), bi.ROUTED_SCALING,
+                                                d["w_post_m"].data_ptr(), d["w_pre_m"].data_ptr(),
+                                                self.T, H, K, n_ffn, bi.EPS, None, st)),
+        )
+        for j, (fn, args) in enumerate(calls):
+            if rec is not None:
+                rec(j).record()
+            stt = getattr(L, fn)(*args)
+            if stt != 0:
+                raise RuntimeError(f"{fn} returned {stt}")
+        if rec is not None:
+            rec(len(calls)).record()
+        return len(calls)
+
+    def outputs(self):
+        d = self.dev
+        return [d["q_r"], d["k_r"], d["q_s"], d["k_s"], self.out_gate, d["h"], self.y, d["h_m"],
+                self.y_m]
+
+
+# ---------------------------------------------------------------------------------------------
+# roofline inputs
+# ---------------------------------------------------------------------------------------------
+
+def measured_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "of measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "of fallback (6.8 TB/s)"
+
+
+def source_hash(name: str) -> str:
+    path = os.path.join(ROOT, "residual_stream_norm_gb300", "csrc", SOURCES[name])
+    h = hashlib.sha256(open(path, "rb").read())
+    dev = os.path.join(ROOT, "residual_stream_norm_gb300", "csrc", "beam_device.cuh")
+    h.update(open(dev, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name: str, T: int):
+    """DRAM bytes per launch from the committed ncu summary, scaled to T tokens; None when the
+    kernel source changed since the counters were taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)[name]
+    except Exception:
+        return None
+    if rec.get("source_sha") != source_hash(name):
+        return None
+    return float(rec["dram_bytes_per_token"]) * T
+
+
+# ---------------------------------------------------------------------------------------------
+# the oracle as CPU baseline
+# ---------------------------------------------------------------------------------------------
+
+def oracle_step(host: dict, lo: int, hi: int, i: int = 0):
+    """The CPU oracle over tokens [lo, hi) of one step (all five operations)."""
+    import oracle
+    u = bi.u16
+    n_attn, n_ffn = 2 * (i % 52) + 1, 2 * (i % 52) + 2
+    wi = (n_attn - 1) % bi.N_BOUNDARIES
+    s = slice(lo, hi)
+    oracle.qk_norm_rope(u(host["q_r"][s]), u(host["k_r"][s]), u(host["wq_r"]), u(host["wk_r"]),
+                        host["pos_r"][s].numpy())
+    oracle.qk_norm_ssmax(u(host["q_s"][s]), u(host["k_s"][s]), u(host["wq_s"]), u(host["wk_s"]),
+                         host["pos_s"][s].numpy())
+    oracle.attn_gate(u(host["attn"][s]), u(host["gate"][s]), host["bias"].numpy(), NQ, D)
+    oracle.boundary(u(host["h"][s]), u(host["x"][s]), u(host["w_post"][wi]), u(host["w_pre"][wi]),
+                    n_attn)
+    oracle.moe_combine_boundary(u(host["h_m"][s]), u(host["e"][s]), host["topk_w"][s].numpy(),
+                                u(host["w_post_m"]), u(host["w_pre_m"]), n_ffn)
+
+
+def time_oracle(host: dict, tokens: int, threads: int, i: int = 0) -> float:
+    import oracle
+    t0 = time.perf_counter()
+    oracle.run_token_parallel(lambda lo, hi: oracle_step(host, lo, hi, i), tokens, threads)
+    return time.perf_counter() - t0
+
+
+# ---------------------------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------------------------
+
+def decode_chain_us(device, replays: int = 200) -> dict:
+    """Batch-1 decode: 104 boundary launches n = 1..104 captured in one CUDA graph."""
+    import residual_stream_norm_gb300 as rsn
+    ch = bi.decode_chain()
+    h = ch["h0"].to(device)
+    xs, wpo, wpr = ch["xs"].to(device), ch["w_post"].to(device), ch["w_pre"].to(device)
+    y = torch.empty((bi.N_BOUNDARIES, 1, H), dtype=torch.bfloat16, device=device)
+    L = rsn.lib()
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    g = torch.cuda.CUDAGraph()
+
+    def chain(stream_handle):
+        for i in range(bi.N_BOUNDARIES):
+            st = L.beam_boundary_fwd(h.data_ptr(), y[i].data_ptr(), h.data_ptr(),
+                                     xs[i].data_ptr(), wpo[i].data_ptr(), wpr[i].data_ptr(), 1, H,
+                                     i + 1, bi.EPS, None, stream_handle)
+            assert st == 0
+    with torch.cuda.stream(s):
+        chain(s.cuda_stream)  # warm
+        with torch.cuda.graph(g, stream=s):
+            chain(s.cuda_stream)
+    torch.cuda.synchronize(device)
+    for _ in range(10):
+        g.replay()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(replays):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize(device)
+    graph_us = e0.elapsed_time(e1) * 1e3 / replays / bi.N_BOUNDARIES
+    # eager launches of the same chain (launch overhead included)
+    e0.record()
+    for _ in range(20):
+        chain(torch.cuda.current_stream(device).cuda_stream)
+    e1.record()
+    torch.cuda.synchronize(device)
+    eager_us = e0.elapsed_time(e1) * 1e3 / 20 / bi.N_BOUNDARIES
+    return {"us_per_boundary": round(graph_us, 3), "boundaries": bi.N_BOUNDARIES,
+            "graph_replays": replays, "eager_us_per_boundary": round(eager_us, 3),
+            "T": 1, "note": "working set fits in L2: time only, no HBM GB/s"}
+
+
+def run_gpu_arm(args) -> None:
+    ws, rank, local = dist_env()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    init_dist(ws, "nccl")
+    import residual_stream_norm_gb300 as rsn
+    rsn.lib()  # fail loudly if the library is not built
+
+    host = make_host_inputs(T_PREFILL, seed=rank)
+    step = Step(host, device)
+    torch.cuda.synchronize(device)
+
+    launches_per_step = 5
+    for i in range(args.warmup):
+        step.launch(i)
+    torch.cuda.synchronize(device)
+
+    nk = len(KERNELS)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler come up before the timed region
+    barrier(ws)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.perf_counter()
+    gpu_launches = 0
+    for i in range(args.steps):
+        gpu_launches += step.launch(i, events=ev[i])
+    torch.cuda.synchronize(device)
+    t_wall1 = time.perf_counter()
+    barrier(ws)
+    clocks.stop()
+
+    total_ms = ev[0][0].elapsed_time(ev[-1][nk])
+    per_kernel_ms = {KERNELS[j]: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
+                     / args.steps for j in range(nk)}
+    max_ms = max_over_ranks(total_ms, ws, device)
+    T = step.T
+    value = ws * T * args.steps / (max_ms * 1e-3)
+
+    peak, peak_src = measured_peak()
+    kernels = {}
+    for name in KERNELS:
+        ms = per_kernel_ms[name]
+        by = BYTES_PER_TOKEN[name] * T
+        gbs = by / (ms * 1e-3) / 1e9
+        kernels[name] = {"us": round(ms * 1e3, 2), "bytes_per_launch": by,
+                         "gb_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+                         "tokens_per_s": round(T / (ms * 1e-3), 1),
+                         "share": round(ms / sum(per_kernel_ms.values()), 4)}
+    dom = max(KERNELS, key=lambda k: per_kernel_ms[k])
+    tr = profiled_traffic(dom, T)
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gb_s"],
+                "peak": peak, "unit": "GB/s", "frac": kernels[dom]["frac_of_peak"],
+                "traffic": tr, "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": kernels[dom]["bytes_per_launch"]}
+
+    # end to end: pinned host -> device, the five kernels, device -> host, every step
+    e2e_steps = min(args.steps, 10)
+    outs = step.outputs()
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in INPUT_KEYS)
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    torch.cuda.synchronize(device)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(e2e_steps):
+        for k in INPUT_KEYS:
+            step.dev[k].copy_(host[k], non_blocking=True)
+        step.launch(i)
+        for o, ho in zip(outs, host_out):
+            ho.copy_(o, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
+    e2e = {"value": round(ws * T * e2e_steps / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "path": "pinned host buffers -> cudaMemcpyAsync -> C ABI -> cudaMemcpyAsync -> host"}
+
+    decode = decode_chain_us(device)
+
+    out = None
+    if rank == 0:
+        threads = os.cpu_count() or 1
+        cpu_s = time_oracle(host, T, threads)
+        cpu = {"value": round(T / cpu_s, 1), "unit": "tokens/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"one full step ({T} tokens through all five operations), "
+                         f"{threads} threads over token slices, {cpu_s:.2f} s wall"}
+        out = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(max_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage": "bf16",
+            "data": "synthetic (seeded, Beam-shaped)",
+            "config": {"workload": "prefill 8x2048 = 16384 tokens at ~100K context: one pass of "
+                                   "qk_norm_rope, qk_norm_ssmax, attn_gate, boundary, "
+                                   "moe_combine_boundary (hidden 5120, 48/8 heads x 128, top-8)",
+                       "tokens_per_step": T, "hidden": H, "top_k": K,
+                       "l2": "inputs larger than L2 (every kernel streams >= 168 MB per launch; "
+                             "L2 129 MB); no flush",
+                       "parallelism": f"replicas x{ws}"},
+            "kernels": kernels, "roofline": roofline, "decode": decode, "e2e": e2e,
+            "cpu_baseline": cpu, "gpu_launches": gpu_launches * ws,
+            "clocks": clocks.summary(t_wall0, t_wall1),
+            "wall_timed_s": round(t_wall1 - t_wall0, 4),
+        }
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference_arm(args) -> None:
+    """The CPU oracle, as it stands, timed on the host cores on the same workload."""
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    threads = os.cpu_count() or 1
+    host = make_host_inputs(T_PREFILL, seed=0)
+    T = T_PREFILL
+    t_first = time_oracle(host, T, threads)
+    # bound the run: at most ~150 s for warmup + steps
+    per_step = max(64, min(T, int(T * 150.0 / max(1e-9, t_first * (args.steps + args.warmup)))))
+    per_step -= per_step % 64
+    for i in range(max(0, args.warmup - 1)):
+        time_oracle(host, per_step, threads, i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        time_oracle(host, per_step, threads, i)
+    el = time.perf_counter() - t0
+    value = per_step * args.steps / el
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage": "bf16",
+        "data": "synthetic (seeded, Beam-shaped)",
+        "config": {"workload": "prefill 8x2048 = 16384 tokens at ~100K context: one pass of "
+                               "qk_norm_rope, qk_norm_ssmax, attn_gate, boundary, "
+                               "moe_combine_boundary (hidden 5120, 48/8 heads x 128, top-8)",
+                   "tokens_per_step": T, "hidden": H, "top_k": K},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"{per_step} of the {T} tokens per step, all five operations"},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference_arm(args)
+    else:
+        run_gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

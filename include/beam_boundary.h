@@ -1,0 +1,193 @@
+/*
+ * beam_boundary.h -- C ABI of the Beam sublayer-boundary library (libbeam_boundary.so, sm_103a).
+ *
+ * The library computes the per-token fused path at the sublayer boundaries of the Beam-1.0
+ * 501B-A23B MoE decoder, and the two attention-side kernels that sit on the same path.
+ *
+ * Pages cited (titles as printed):
+ *   [vLLM]  "Serving Reflection Beam auf vLLM ab Tag 0"
+ *   [SGL]   "SGLang 支撑编程模型 Beam 生产部署"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - BF16 tensors are passed as `void*` to IEEE bfloat16 storage; FP32 tensors as `float*`.
+ *  - Every pointer is a device pointer on the CURRENT CUDA device.  The caller allocates, owns
+ *    and frees every buffer; the library never allocates, frees or synchronises.
+ *  - Every call is asynchronous on `stream` (0 = the legacy default stream).  The returned status
+ *    reflects the argument checks and `cudaGetLastError()` right after the launch; a fault that
+ *    happens later surfaces on the next synchronising CUDA call, as for any kernel.
+ *  - Arguments are validated before anything is launched; on any error nothing is launched and
+ *    no output is touched.  T == 0 returns BEAM_OK without launching (pointers may then be NULL).
+ *  - Alignment: every BF16 pointer 16-byte aligned, row strides multiples of 8 elements (16 B),
+ *    `float*` / `int64_t*` arrays aligned to their element size (the per-token FP32 pair
+ *    `rstd_out` to 8 bytes).  Violations return BEAM_ERR_MISALIGNED.
+ *  - Arithmetic is FP32 with IEEE division and square root; results are rounded to BF16 with
+ *    round-to-nearest-even exactly at the points each call lists.
+ *  - Aliasing: only the overlaps each call names are allowed; any other overlap is undefined.
+ */
+#ifndef BEAM_BOUNDARY_H
+#define BEAM_BOUNDARY_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define BEAM_ABI_VERSION 1
+
+/* Symbols of this header are the library's only exported symbols. */
+#if defined(__GNUC__)
+#define BEAM_API __attribute__((visibility("default")))
+#else
+#define BEAM_API
+#endif
+
+typedef enum {
+    BEAM_OK = 0,
+    BEAM_ERR_INVALID_ARG = -1,  /* NULL pointer, negative size, out-of-range parameter        */
+    BEAM_ERR_MISALIGNED = -2,   /* pointer or stride not aligned as the conventions require     */
+    BEAM_ERR_UNSUPPORTED = -3,  /* a shape the kernels do not implement (e.g. head_dim != 128)  */
+    BEAM_ERR_CUDA = -4          /* the launch failed; see cudaGetLastError() semantics above    */
+} beam_status_t;
+
+/* BEAM_ABI_VERSION of the loaded library. */
+BEAM_API int beam_abi_version(void);
+
+/* Static, NUL-terminated name of a status code ("BEAM_OK", ...; "unknown" otherwise). */
+BEAM_API const char *beam_status_str(int status);
+
+/* Host-only helper: the FP32 coefficients the boundary calls use for residual index n >= 1,
+ * alpha = fp32(sqrt((n-1)/n)) and s = fp32(sqrt(n)), each computed in double and rounded once.
+ * [vLLM] "MoE und Residual-Stream", bullet "Tiefenskalierte Residuen".
+ * Returns BEAM_ERR_INVALID_ARG for n < 1 or NULL outputs. */
+BEAM_API int beam_residual_scales(int32_t n, float *alpha, float *s);
+
+/* Host-only helper: the FP32 cosine and sine that beam_qk_norm_rope_fwd uses for an FP32 rotary
+ * angle, for `count` angles in host memory.  Each value is the FP32 rounding of the exact
+ * cos / sin of the FP32 angle (except in rare near-tie cases), computed in FP32 pair arithmetic
+ * (Cody-Waite reduction, Dekker products, Taylor series).  Angles must satisfy |a| < 2^24;
+ * others give NaN outputs and BEAM_ERR_INVALID_ARG.  Returns BEAM_ERR_INVALID_ARG for NULL
+ * arrays (count > 0) or count < 0. */
+BEAM_API int beam_rope_cos_sin(const float *angle, float *cos_out, float *sin_out, int64_t count);
+
+/* Sublayer boundary: post-RMSNorm -> depth-scaled residual add -> next pre-RMSNorm, per token.
+ *
+ * Defined by [vLLM] "MoE und Residual-Stream" (bullets "Sandwich-Norm": an RMSNorm before and
+ * after every sublayer; "Tiefenskalierte Residuen": the n-th residual add is
+ * h <- sqrt((n-1)/n) h + x/sqrt(n)), [vLLM] "Agentengetriebene Optimierung" change 1 (the three
+ * steps fused at each of the 104 boundaries, FP32 math, the reference BF16 rounding points) and
+ * [SGL] "三明治归一化与深度缩放残差" (both scaled operands rounded to BF16 before the add).
+ *
+ * For every token t (row of H elements), with m(v) = fp32(sum_j fp32(v_j^2)) / H:
+ *   r     = 1 / sqrt(m(x) + eps)
+ *   xhat  = bf16((x * r) * w_post)                      post-norm of the sublayer output
+ *   a     = bf16(alpha * h),  b = bf16(xhat / s),  h' = bf16(a + b)
+ *   r'    = 1 / sqrt(m(h') + eps)
+ *   y     = bf16((h' * r') * w_pre)                     pre-norm of the next sublayer
+ * with alpha, s from beam_residual_scales(n).  The sum of squares is formed to within ~1e-11
+ * relative of its exact value before its single FP32 rounding.
+ *
+ *   h_out  [T, H] bf16  out: h'              (may be the same buffer as h_in)
+ *   y_out  [T, H] bf16  out: y               (may be the same buffer as x_in)
+ *   h_in   [T, H] bf16  residual stream before the add
+ *   x_in   [T, H] bf16  sublayer output (before its post-norm)
+ *   w_post [H]    bf16  post-norm weight of the sublayer;  w_pre [H] bf16 next pre-norm weight
+ *   T >= 0 tokens; H hidden size, a multiple of 8 in [8, 16384]; n >= 1 residual index;
+ *   eps >= 0 and finite;
+ *   rstd_out [T, 2] fp32 or NULL: (r, r') per token.
+ * Rows are contiguous (row stride H). */
+BEAM_API int beam_boundary_fwd(void *h_out, void *y_out, const void *h_in, const void *x_in,
+                      const void *w_post, const void *w_pre, int64_t T, int32_t H, int32_t n,
+                      float eps, float *rstd_out, cudaStream_t stream);
+
+/* MoE top-K combine fused ahead of the boundary chain.
+ *
+ * [vLLM] "MoE und Residual-Stream", bullet "MoE im DeepSeek-V3-Stil" (top-8 experts, the
+ * renormalised weights scaled by 2.5); [vLLM] "Agentengetriebene Optimierung" change 3 (the
+ * boundary kernel also combines the top-8 expert outputs); [SGL] "稠密层与分组 MoE 路由"
+ * (routing coefficients kept in FP32 and the scale applied in the combine) and its
+ * kernel-fusion paragraph (expert sum, routing scale and BF16 rounding in one place).
+ *
+ * Per token: c_k = fp32(topk_w[t,k] * routed_scaling);
+ *   x_j = bf16(acc), acc = fma(c_{K-1}, e_{K-1,j}, ... fma(c_1, e_{1,j}, fma(c_0, e_{0,j}, +0)))
+ * i.e. one FP32 fused multiply-add per slot in slot order 0..K-1; then exactly the
+ * beam_boundary_fwd chain on x.
+ *
+ *   expert_out [T, K, H] bf16  the K selected experts' outputs per token, slot-major per token
+ *   topk_w     [T, K]    fp32  renormalised routing weights (renormalisation is the caller's)
+ *   routed_scaling             finite (2.5 for Beam);  K in [1, 16]
+ *   other arguments as beam_boundary_fwd (h_out may equal h_in; no other overlap). */
+BEAM_API int beam_moe_combine_boundary_fwd(void *h_out, void *y_out, const void *h_in,
+                                  const void *expert_out, const float *topk_w,
+                                  float routed_scaling, const void *w_post, const void *w_pre,
+                                  int64_t T, int32_t H, int32_t K, int32_t n, float eps,
+                                  float *rstd_out, cudaStream_t stream);
+
+/* Per-head Q/K RMSNorm fused with rotary embedding (sliding-window layers), in place.
+ *
+ * [vLLM] "Attention", bullets "GQA mit Per-Head-Q/K-Norm" (48 query heads, 8 KV heads, head
+ * dimension 128; Q and K RMS-normalised per head before RoPE or SSMax) and "Hybride
+ * Sliding-Window- und NoPE-Schichten" (RoPE on the sliding-window layers); [SGL] kernel-fusion
+ * paragraph (sliding-window layers fuse the Q/K norm with RoPE).
+ *
+ * Per token t and head (row v of 128 elements, weight w = wq for Q heads, wk for K heads):
+ *   r = 1 / sqrt(m(v) + eps);  qhat_d = (v_d * r) * w_d   (FP32, not rounded)
+ *   angle_i = fp32(fp32(pos[t]) * inv_freq_i),  inv_freq_i = fp32(theta^(-2i/128)), i < 64
+ *   out_i    = bf16( fp32(qhat_i * cos_i)    - fp32(qhat_{i+64} * sin_i) )
+ *   out_{i+64} = bf16( fp32(qhat_{i+64} * cos_i) + fp32(qhat_i * sin_i) )
+ * cos_i / sin_i are the FP32 roundings of the exact cosine and sine of the FP32 angle
+ * (beam_rope_cos_sin) when |angle_i| < 2^24 (always, for positions < 2^24 and theta >= 1);
+ * larger angles use CUDA's sincosf (within 2 FP32 ulps).
+ *
+ *   q [T, n_q_heads, 128] bf16 in place, row t at q + t*q_row_stride (elements)
+ *   k [T, n_kv_heads, 128] bf16 in place, row t at k + t*k_row_stride
+ *   wq, wk [128] bf16 norm weights (shared by all heads of Q, resp. K)
+ *   pos [T] int64, 0-based positions >= 0 (converted to FP32; exact below 2^24)
+ *   n_q_heads, n_kv_heads >= 0 with n_q_heads + n_kv_heads in [1, 1024]; head_dim must be 128
+ *   (else BEAM_ERR_UNSUPPORTED); eps >= 0; theta > 0.  q (k) may be NULL when n_q_heads
+ *   (n_kv_heads) is 0.  Strides >= the row length and multiples of 8, so Q and K may be views
+ *   into one packed QKV(+gate) projection output; q and k rows must not overlap. */
+BEAM_API int beam_qk_norm_rope_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride,
+                          const void *wq, const void *wk, const int64_t *pos, int64_t T,
+                          int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, float eps,
+                          float theta, cudaStream_t stream);
+
+/* Per-head Q/K RMSNorm fused with the SSMax query scale (NoPE layers), in place.
+ *
+ * [vLLM] "Attention", bullet "SSMax auf NoPE-Schichten" (each query scaled by (1 + p/2048)^0.1,
+ * p the 1-based position); [SGL] "稠密层与分组 MoE 路由", SSMax paragraph (after the Q/K norm,
+ * the query at 0-based position p is scaled by (1 + (p+1)/2048)^0.1).
+ *
+ * Q heads: out = bf16( ((v * r) * wq) * sigma_t ),  sigma_t = fp32((1 + (pos[t]+1)/base)^expo)
+ * evaluated in double and rounded once;  K heads: out = bf16( (v * r) * wk ) (no scale).
+ * Arguments as beam_qk_norm_rope_fwd; ssmax_base > 0 (2048), ssmax_exp finite (0.1). */
+BEAM_API int beam_qk_norm_ssmax_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride,
+                           const void *wq, const void *wk, const int64_t *pos, int64_t T,
+                           int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, float eps,
+                           float ssmax_base, float ssmax_exp, cudaStream_t stream);
+
+/* Sigmoid attention-output gate, before the output projection.
+ *
+ * [vLLM] "Attention", bullet "Sigmoid-Output-Gate" (each head's output times
+ * sigma(gate + bias) with a learned per-head bias; a head can be switched off token by token);
+ * [SGL] "混合注意力与输出门控" and the kernel-fusion paragraph (bias add, sigmoid and multiply
+ * fused in one kernel).
+ *
+ * out[t, h*D + d] = bf16( attn * (1 / (1 + expf(-z))) ),  z = fp32(gate[t, h*D + d] + bias[h]),
+ * with CUDA's full-accuracy expf, FP32 add and IEEE division.
+ *
+ *   out, attn, gate  [T, n_heads*head_dim] bf16 rows at the given strides (elements, >= the row
+ *   length, multiples of 8); out may be the same buffer as attn (same stride) for in-place use.
+ *   bias [n_heads] fp32 (+-inf allowed: -inf switches a head off, +inf passes it through).
+ *   n_heads in [1, 1024]; head_dim a multiple of 8 in [8, 1024]. */
+BEAM_API int beam_attn_gate_fwd(void *out, const void *attn, const void *gate, const float *bias,
+                       int64_t T, int32_t n_heads, int32_t head_dim, int64_t attn_row_stride,
+                       int64_t gate_row_stride, int64_t out_row_stride, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BEAM_BOUNDARY_H */

@@ -1,0 +1,263 @@
+// beam_api.cu -- C ABI of libbeam_boundary.so: argument checks, host-side coefficients, launch.
+//
+// Every check runs before any CUDA call, so a rejected call launches nothing, touches no output
+// and needs no GPU.  The library holds no state besides a small per-thread cache of RoPE
+// frequency tables; it never allocates device memory and never synchronises.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/beam_boundary.h"
+#include "beam_kernels.h"
+#include "beam_sincos.cuh"
+
+namespace {
+
+constexpr int32_t kMaxHidden = 16384;
+constexpr int32_t kMaxK = 16;
+constexpr int32_t kHeadDim = 128;
+constexpr int32_t kMaxHeads = 1024;
+
+inline bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? BEAM_OK : BEAM_ERR_CUDA; }
+
+int check_hidden(int32_t H) { return (H < 8 || H > kMaxHidden || H % 8 != 0) ? BEAM_ERR_INVALID_ARG : BEAM_OK; }
+
+bool bad_eps(float eps) { return !(eps >= 0.0f) || !std::isfinite(eps); }
+
+// fp32(theta^(-2i/128)) for i < 64, formed in double.  Cached per thread for the last theta.
+const float *rope_inv_freq(float theta)
+{
+    static thread_local float cached_theta = -1.0f;
+    static thread_local float table[kHeadDim / 2];
+    if (cached_theta != theta) {
+        for (int i = 0; i < kHeadDim / 2; ++i)
+            table[i] = (float)std::pow((double)theta, -2.0 * (double)i / (double)kHeadDim);
+        cached_theta = theta;
+    }
+    return table;
+}
+
+int check_qk(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride, const void *wq,
+             const void *wk, const int64_t *pos, int64_t T, int32_t n_q, int32_t n_kv,
+             int32_t head_dim, float eps)
+{
+    if (head_dim != kHeadDim)
+        return BEAM_ERR_UNSUPPORTED;
+    if (T < 0 || n_q < 0 || n_kv < 0 || n_q + n_kv < 1 || n_q + n_kv > kMaxHeads || bad_eps(eps))
+        return BEAM_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_OK;
+    if (!pos || (n_q > 0 && (!q || !wq)) || (n_kv > 0 && (!k || !wk)))
+        return BEAM_ERR_INVALID_ARG;
+    if ((n_q > 0 && q_row_stride < (int64_t)n_q * kHeadDim) ||
+        (n_kv > 0 && k_row_stride < (int64_t)n_kv * kHeadDim))
+        return BEAM_ERR_INVALID_ARG;
+    if ((n_q > 0 && (!aligned(q, 16) || !aligned(wq, 16) || q_row_stride % 8 != 0)) ||
+        (n_kv > 0 && (!aligned(k, 16) || !aligned(wk, 16) || k_row_stride % 8 != 0)) ||
+        !aligned(pos, 8))
+        return BEAM_ERR_MISALIGNED;
+    return BEAM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int beam_abi_version(void) { return BEAM_ABI_VERSION; }
+
+const char *beam_status_str(int status)
+{
+    switch (status) {
+    case BEAM_OK: return "BEAM_OK";
+    case BEAM_ERR_INVALID_ARG: return "BEAM_ERR_INVALID_ARG";
+    case BEAM_ERR_MISALIGNED: return "BEAM_ERR_MISALIGNED";
+    case BEAM_ERR_UNSUPPORTED: return "BEAM_ERR_UNSUPPORTED";
+    case BEAM_ERR_CUDA: return "BEAM_ERR_CUDA";
+    default: return "unknown";
+    }
+}
+
+int beam_residual_scales(int32_t n, float *alpha, float *s)
+{
+    if (n < 1 || !alpha || !s)
+        return BEAM_ERR_INVALID_ARG;
+    *alpha = (float)std::sqrt((double)(n - 1) / (double)n);
+    *s = (float)std::sqrt((double)n);
+    return BEAM_OK;
+}
+
+int beam_rope_cos_sin(const float *angle, float *cos_out, float *sin_out, int64_t count)
+{
+    if (count < 0 || (count > 0 && (!angle || !cos_out || !sin_out)))
+        return BEAM_ERR_INVALID_ARG;
+    int st = BEAM_OK;
+    for (int64_t i = 0; i < count; ++i) {
+        const float x = angle[i];
+        if (!(std::fabs(x) < beam::kSinCosMaxArg)) {
+            cos_out[i] = sin_out[i] = NAN;
+            st = BEAM_ERR_INVALID_ARG;
+            continue;
+        }
+        beam::sincos_rounded(x, &sin_out[i], &cos_out[i]);
+    }
+    return st;
+}
+
+int beam_boundary_fwd(void *h_out, void *y_out, const void *h_in, const void *x_in,
+                      const void *w_post, const void *w_pre, int64_t T, int32_t H, int32_t n,
+                      float eps, float *rstd_out, cudaStream_t stream)
+{
+    if (T < 0 || n < 1 || bad_eps(eps) || check_hidden(H) != BEAM_OK)
+        return BEAM_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_OK;
+    if (!h_out || !y_out || !h_in || !x_in || !w_post || !w_pre)
+        return BEAM_ERR_INVALID_ARG;
+    if (!aligned(h_out, 16) || !aligned(y_out, 16) || !aligned(h_in, 16) || !aligned(x_in, 16) ||
+        !aligned(w_post, 16) || !aligned(w_pre, 16) || (rstd_out && !aligned(rstd_out, 8)))
+        return BEAM_ERR_MISALIGNED;
+    beam::BoundaryArgs a{};
+    a.h_out = h_out;
+    a.y_out = y_out;
+    a.h_in = h_in;
+    a.x_in = x_in;
+    a.w_post = w_post;
+    a.w_pre = w_pre;
+    a.rstd_out = rstd_out;
+    a.T = T;
+    a.H = H;
+    a.K = 0;
+    a.eps = eps;
+    beam_residual_scales(n, &a.alpha, &a.s);
+    return cuda_status(beam::launch_boundary(a, stream));
+}
+
+int beam_moe_combine_boundary_fwd(void *h_out, void *y_out, const void *h_in,
+                                  const void *expert_out, const float *topk_w,
+                                  float routed_scaling, const void *w_post, const void *w_pre,
+                                  int64_t T, int32_t H, int32_t K, int32_t n, float eps,
+                                  float *rstd_out, cudaStream_t stream)
+{
+    if (T < 0 || n < 1 || K < 1 || K > kMaxK || bad_eps(eps) || !std::isfinite(routed_scaling) ||
+        check_hidden(H) != BEAM_OK)
+        return BEAM_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_OK;
+    if (!h_out || !y_out || !h_in || !expert_out || !topk_w || !w_post || !w_pre)
+        return BEAM_ERR_INVALID_ARG;
+    if (!aligned(h_out, 16) || !aligned(y_out, 16) || !aligned(h_in, 16) ||
+        !aligned(expert_out, 16) || !aligned(topk_w, 4) || !aligned(w_post, 16) ||
+        !aligned(w_pre, 16) || (rstd_out && !aligned(rstd_out, 8)))
+        return BEAM_ERR_MISALIGNED;
+    beam::BoundaryArgs a{};
+    a.h_out = h_out;
+    a.y_out = y_out;
+    a.h_in = h_in;
+    a.expert_out = expert_out;
+    a.topk_w = topk_w;
+    a.routed_scaling = routed_scaling;
+    a.w_post = w_post;
+    a.w_pre = w_pre;
+    a.rstd_out = rstd_out;
+    a.T = T;
+    a.H = H;
+    a.K = K;
+    a.eps = eps;
+    beam_residual_scales(n, &a.alpha, &a.s);
+    return cuda_status(beam::launch_moe_boundary(a, stream));
+}
+
+int beam_qk_norm_rope_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride,
+                          const void *wq, const void *wk, const int64_t *pos, int64_t T,
+                          int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, float eps,
+                          float theta, cudaStream_t stream)
+{
+    int st = check_qk(q, k, q_row_stride, k_row_stride, wq, wk, pos, T, n_q_heads, n_kv_heads,
+                      head_dim, eps);
+    if (st != BEAM_OK)
+        return st;
+    if (!(theta > 0.0f) || !std::isfinite(theta))
+        return BEAM_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_OK;
+    beam::QkArgs a{};
+    a.q = q;
+    a.k = k;
+    a.q_stride = q_row_stride;
+    a.k_stride = k_row_stride;
+    a.wq = wq;
+    a.wk = wk;
+    a.pos = pos;
+    a.T = T;
+    a.n_q = n_q_heads;
+    a.n_kv = n_kv_heads;
+    a.eps = eps;
+    a.inv_freq_host = rope_inv_freq(theta);
+    return cuda_status(beam::launch_qk_norm_rope(a, stream));
+}
+
+int beam_qk_norm_ssmax_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride,
+                           const void *wq, const void *wk, const int64_t *pos, int64_t T,
+                           int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, float eps,
+                           float ssmax_base, float ssmax_exp, cudaStream_t stream)
+{
+    int st = check_qk(q, k, q_row_stride, k_row_stride, wq, wk, pos, T, n_q_heads, n_kv_heads,
+                      head_dim, eps);
+    if (st != BEAM_OK)
+        return st;
+    if (!(ssmax_base > 0.0f) || !std::isfinite(ssmax_base) || !std::isfinite(ssmax_exp))
+        return BEAM_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_OK;
+    beam::QkArgs a{};
+    a.q = q;
+    a.k = k;
+    a.q_stride = q_row_stride;
+    a.k_stride = k_row_stride;
+    a.wq = wq;
+    a.wk = wk;
+    a.pos = pos;
+    a.T = T;
+    a.n_q = n_q_heads;
+    a.n_kv = n_kv_heads;
+    a.eps = eps;
+    a.ssmax_base = ssmax_base;
+    a.ssmax_exp = ssmax_exp;
+    return cuda_status(beam::launch_qk_norm_ssmax(a, stream));
+}
+
+int beam_attn_gate_fwd(void *out, const void *attn, const void *gate, const float *bias,
+                       int64_t T, int32_t n_heads, int32_t head_dim, int64_t attn_row_stride,
+                       int64_t gate_row_stride, int64_t out_row_stride, cudaStream_t stream)
+{
+    if (head_dim < 8 || head_dim > 1024 || head_dim % 8 != 0)
+        return BEAM_ERR_UNSUPPORTED;
+    if (T < 0 || n_heads < 1 || n_heads > kMaxHeads)
+        return BEAM_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_OK;
+    const int64_t C = (int64_t)n_heads * head_dim;
+    if (!out || !attn || !gate || !bias || attn_row_stride < C || gate_row_stride < C ||
+        out_row_stride < C)
+        return BEAM_ERR_INVALID_ARG;
+    if (!aligned(out, 16) || !aligned(attn, 16) || !aligned(gate, 16) || !aligned(bias, 4) ||
+        attn_row_stride % 8 != 0 || gate_row_stride % 8 != 0 || out_row_stride % 8 != 0)
+        return BEAM_ERR_MISALIGNED;
+    beam::GateArgs a{};
+    a.out = out;
+    a.attn = attn;
+    a.gate = gate;
+    a.bias = bias;
+    a.T = T;
+    a.n_heads = n_heads;
+    a.head_dim = head_dim;
+    a.attn_stride = attn_row_stride;
+    a.gate_stride = gate_row_stride;
+    a.out_stride = out_row_stride;
+    return cuda_status(beam::launch_attn_gate(a, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,164 @@
+// beam_device.cuh -- device helpers shared by the Beam boundary-path kernels (sm_103a).
+//
+// All rounding-sensitive arithmetic uses the explicit IEEE round-to-nearest intrinsics
+// (__fadd_rn, __fmul_rn, ...) so that no multiply-add contraction or reassociation can change
+// a result; the library is also compiled with -fmad=false.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace beam {
+
+// ---------------------------------------------------------------------------------------------
+// BF16 <-> FP32.  A 32-bit word holds two BF16 values: element 2i in the low half, 2i+1 high.
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Round two FP32 values to BF16 (IEEE round-to-nearest-even, NaN preserved) and pack them.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Global memory access.  16-byte vectors.  Streamed tensors bypass L1 allocation and use the
+// coherent path (an output may be the same buffer as an input); small tensors that are
+// read-only for the whole kernel (norm weights) use the non-coherent path with L1 caching.  The
+// loads are volatile so that they are never moved past a store of the same kernel.
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint4 ld_stream(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ld_cached(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Coherent load, for data this kernel may also write (in-place Q/K rows, in-place gate).
+__device__ __forceinline__ uint4 ld_plain(const void *p)
+{
+    uint4 v;
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_global(void *p, uint4 v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t &word(uint4 &v, int i)
+{
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+__device__ __forceinline__ uint32_t word(const uint4 &v, int i)
+{
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Compensated sum of non-negative FP32 terms.
+//
+// (hi, lo) carries a running sum whose rounding errors are captured exactly by Knuth's TwoSum
+// (an error-free transformation: s + e == a + b exactly).  The final hi + lo is the FP32
+// rounding of a value within ~n * 2^-48 relative of the exact sum, so the rounded result is
+// the correctly rounded sum except in vanishingly rare near-tie cases -- the summation order
+// (thread, warp, block) no longer decides the FP32 result.
+// ---------------------------------------------------------------------------------------------
+
+struct Sum2 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = __fadd_rn(a, b);
+    float bp = __fsub_rn(s, a);
+    float ap = __fsub_rn(s, bp);
+    e = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
+}
+
+__device__ __forceinline__ void sum_add(Sum2 &acc, float t)
+{
+    float s, e;
+    two_sum(acc.hi, t, s, e);
+    acc.hi = s;
+    acc.lo = __fadd_rn(acc.lo, e);
+}
+
+// Commutative merge: merge(a, b) and merge(b, a) give identical bits, so butterfly shuffles
+// leave every lane with the same value.
+__device__ __forceinline__ Sum2 sum_merge(Sum2 a, Sum2 b)
+{
+    Sum2 r;
+    float e;
+    two_sum(a.hi, b.hi, r.hi, e);
+    r.lo = __fadd_rn(__fadd_rn(a.lo, b.lo), e);
+    return r;
+}
+
+// FP32 value of the sum.  Once hi has overflowed (or a term was inf / NaN) the error term is
+// meaningless (inf - inf); hi alone then carries the IEEE result.
+__device__ __forceinline__ float sum_value(Sum2 a)
+{
+    return isfinite(a.hi) ? __fadd_rn(a.hi, a.lo) : a.hi;
+}
+
+__device__ __forceinline__ Sum2 warp_sum(Sum2 a, int width = 32)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        if (off < width) {
+            Sum2 o;
+            o.hi = __shfl_xor_sync(0xffffffffu, a.hi, off);
+            o.lo = __shfl_xor_sync(0xffffffffu, a.lo, off);
+            a = sum_merge(a, o);
+        }
+    }
+    return a;
+}
+
+// Block-wide sum; `slot` is a shared array of >= blockDim.x/32 entries that no other
+// reduction of the same phase uses.  Every thread returns the same value.
+__device__ __forceinline__ float block_sum(Sum2 a, Sum2 *slot)
+{
+    a = warp_sum(a);
+    const int nw = blockDim.x >> 5;
+    if ((threadIdx.x & 31) == 0)
+        slot[threadIdx.x >> 5] = a;
+    __syncthreads();
+    Sum2 r = slot[0];
+    for (int w = 1; w < nw; ++w)
+        r = sum_merge(r, slot[w]);
+    return sum_value(r);
+}
+
+// r = 1 / sqrt(ms / len + eps) with IEEE division and square root.
+__device__ __forceinline__ float rms_inv(float ms, float len, float eps)
+{
+    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ms, len), eps)));
+}
+
+}  // namespace beam

@@ -1,0 +1,67 @@
+// beam_kernels.h -- internal launch interface between the C ABI (beam_api.cu) and the kernels.
+// Arguments arrive here already validated; launchers only pick a configuration and launch.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace beam {
+
+struct BoundaryArgs {
+    void *h_out;
+    void *y_out;
+    const void *h_in;
+    const void *x_in;        // boundary: sublayer output [T, H]
+    const void *expert_out;  // MoE: [T, K, H] (x_in unused)
+    const float *topk_w;     // MoE: [T, K]
+    const void *w_post;
+    const void *w_pre;
+    float *rstd_out;         // [T, 2] or nullptr
+    int64_t T;
+    int32_t H;
+    int32_t K;               // 0 for the plain boundary
+    float routed_scaling;
+    float alpha;             // fp32(sqrt((n-1)/n))
+    float s;                 // fp32(sqrt(n))
+    float eps;
+};
+
+struct QkArgs {
+    void *q;
+    void *k;
+    int64_t q_stride;  // elements
+    int64_t k_stride;
+    const void *wq;
+    const void *wk;
+    const int64_t *pos;
+    int64_t T;
+    int32_t n_q;
+    int32_t n_kv;
+    float eps;
+    // RoPE
+    const float *inv_freq_host;  // [64], host memory, copied into the launch parameters
+    // SSMax
+    float ssmax_base;
+    float ssmax_exp;
+};
+
+struct GateArgs {
+    void *out;
+    const void *attn;
+    const void *gate;
+    const float *bias;
+    int64_t T;
+    int32_t n_heads;
+    int32_t head_dim;
+    int64_t attn_stride;
+    int64_t gate_stride;
+    int64_t out_stride;
+};
+
+cudaError_t launch_boundary(const BoundaryArgs &a, cudaStream_t stream);
+cudaError_t launch_moe_boundary(const BoundaryArgs &a, cudaStream_t stream);
+cudaError_t launch_qk_norm_rope(const QkArgs &a, cudaStream_t stream);
+cudaError_t launch_qk_norm_ssmax(const QkArgs &a, cudaStream_t stream);
+cudaError_t launch_attn_gate(const GateArgs &a, cudaStream_t stream);
+
+}  // namespace beam

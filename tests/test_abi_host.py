@@ -1,0 +1,191 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+The library must load on a machine without a GPU, export every entry point the header declares,
+and reject every invalid argument with the documented status before any CUDA call -- these
+calls never launch, so they run here with fake (never dereferenced) device addresses.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import residual_stream_norm_gb300 as rsn
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "beam_boundary.h")
+
+OK, INVALID, MISALIGNED, UNSUPPORTED = 0, -1, -2, -3
+A = 0x10000      # a 16-byte aligned fake device address (never dereferenced)
+B = 0x20000
+U = 0x30008      # 8-byte aligned only
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rsn.build()
+    return rsn.lib()
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    return re.findall(r"BEAM_API\s+[\w\s\*]*?\b(beam_\w+)\s*\(", text)
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) == 9, names
+    raw = ctypes.CDLL(rsn.LIB_PATH)
+    for nm in names:
+        assert hasattr(raw, nm), f"{nm} declared in the header but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert rsn.beam_abi_version() == 1
+    assert rsn.beam_status_str(0) == "BEAM_OK"
+    assert rsn.beam_status_str(-2) == "BEAM_ERR_MISALIGNED"
+    assert rsn.beam_status_str(42) == "unknown"
+
+
+def test_residual_scales_match_oracle(lib):
+    for n in list(range(1, 4097)) + [10**5, 2**20, 2**31 - 1]:
+        assert rsn.beam_residual_scales(n) == oracle.residual_scales(n), n
+    with pytest.raises(rsn.BeamError):
+        rsn.beam_residual_scales(0)
+
+
+def boundary(lib, h_out=A, y_out=B, h_in=A, x_in=B, wpo=A, wpr=B, T=4, H=5120, n=5, eps=1e-6,
+             rstd=None):
+    return lib.beam_boundary_fwd(h_out, y_out, h_in, x_in, wpo, wpr, T, H, n, eps, rstd, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(T=-1), INVALID), (dict(n=0), INVALID), (dict(H=0), INVALID), (dict(H=12), INVALID),
+    (dict(H=16392), INVALID), (dict(eps=-1.0), INVALID), (dict(eps=float("nan")), INVALID),
+    (dict(eps=float("inf")), INVALID), (dict(h_out=None), INVALID), (dict(x_in=None), INVALID),
+    (dict(wpr=None), INVALID), (dict(h_in=A + 8), MISALIGNED), (dict(y_out=B + 2), MISALIGNED),
+    (dict(wpo=A + 4), MISALIGNED), (dict(rstd=U + 4), MISALIGNED),
+    (dict(T=0, h_out=None, y_out=None, h_in=None, x_in=None, wpo=None, wpr=None), OK),
+])
+def test_boundary_argument_checks(lib, kw, want):
+    assert boundary(lib, **kw) == want
+
+
+def moe(lib, K=8, topk=A, scale=2.5, T=4, e=B, **kw):
+    return lib.beam_moe_combine_boundary_fwd(A, B, A, e, topk, scale, A, B, T, 5120, K, 5, 1e-6,
+                                             None, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(K=0), INVALID), (dict(K=17), INVALID), (dict(scale=float("inf")), INVALID),
+    (dict(topk=None), INVALID), (dict(e=None), INVALID), (dict(topk=A + 2), MISALIGNED),
+    (dict(e=B + 8), MISALIGNED), (dict(T=0), OK),
+])
+def test_moe_argument_checks(lib, kw, want):
+    assert moe(lib, **kw) == want
+
+
+def qk(lib, fn="rope", q=A, k=B, qs=48 * 128, ks=8 * 128, pos=U, T=4, nq=48, nk=8, D=128,
+       eps=1e-6, extra=(10000.0,)):
+    f = lib.beam_qk_norm_rope_fwd if fn == "rope" else lib.beam_qk_norm_ssmax_fwd
+    return f(q, k, qs, ks, A, B, pos, T, nq, nk, D, eps, *extra, None)
+
+
+@pytest.mark.parametrize("fn,extra", [("rope", (10000.0,)), ("ssmax", (2048.0, 0.1))])
+@pytest.mark.parametrize("kw,want", [
+    (dict(D=64), UNSUPPORTED), (dict(D=256), UNSUPPORTED), (dict(T=-3), INVALID),
+    (dict(nq=0, nk=0), INVALID), (dict(nq=-1), INVALID), (dict(nq=1000, nk=100), INVALID),
+    (dict(pos=None), INVALID), (dict(q=None), INVALID), (dict(qs=48 * 128 - 8), INVALID),
+    (dict(q=A + 8), MISALIGNED), (dict(qs=48 * 128 + 4), MISALIGNED),
+    (dict(ks=8 * 128 + 2), MISALIGNED), (dict(pos=U + 4), MISALIGNED),
+    (dict(T=0, q=None, k=None, pos=None), OK), (dict(nq=0, q=None, T=0), OK),
+])
+def test_qk_argument_checks(lib, fn, extra, kw, want):
+    assert qk(lib, fn=fn, extra=extra, **kw) == want
+
+
+def test_qk_parameter_checks(lib):
+    assert qk(lib, fn="rope", extra=(0.0,)) == INVALID
+    assert qk(lib, fn="rope", extra=(float("nan"),)) == INVALID
+    assert qk(lib, fn="ssmax", extra=(0.0, 0.1)) == INVALID
+    assert qk(lib, fn="ssmax", extra=(2048.0, float("inf"))) == INVALID
+
+
+def gate(lib, out=A, attn=A, g=B, bias=U, T=4, nh=48, D=128, sa=6144, sg=6144, so=6144):
+    return lib.beam_attn_gate_fwd(out, attn, g, bias, T, nh, D, sa, sg, so, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(D=12), UNSUPPORTED), (dict(D=0), UNSUPPORTED), (dict(D=2048), UNSUPPORTED),
+    (dict(nh=0), INVALID), (dict(T=-1), INVALID), (dict(bias=None), INVALID),
+    (dict(sa=6136), INVALID), (dict(out=A + 8), MISALIGNED), (dict(bias=U + 2), MISALIGNED),
+    (dict(sg=6148), MISALIGNED), (dict(T=0, out=None, attn=None, g=None, bias=None), OK),
+])
+def test_gate_argument_checks(lib, kw, want):
+    assert gate(lib, **kw) == want
+
+
+def test_rejected_calls_raise_in_the_binding(lib):
+    with pytest.raises(rsn.BeamError) as e:
+        rsn._call("beam_boundary_fwd", A, B, A, B, A, B, 4, 12, 5, 1e-6, None, None)
+    assert e.value.status == INVALID
+
+
+# ------------------------------------------------------------------------------------------
+# the RoPE cos / sin routine (host build of the device code)
+# ------------------------------------------------------------------------------------------
+
+def _rounded(x32):
+    x = x32.astype(np.float64)
+    return np.cos(x).astype(np.float32), np.sin(x).astype(np.float32)
+
+
+def _check_rounded(angles, what, tiny=2.0 ** -20):
+    c, s = rsn.beam_rope_cos_sin(angles)
+    wc, ws = _rounded(angles)
+    for got, want in ((c, wc), (s, ws)):
+        bad = got != want
+        # a miss may only be a near tie of a tiny value (whose absolute error is ~2^-47)
+        assert not np.any(bad & (np.abs(want) >= tiny)), (what, angles[bad][:5], got[bad][:5],
+                                                          want[bad][:5])
+        assert np.mean(bad) < 1e-6, (what, np.mean(bad))
+        if np.any(bad):
+            ulps = np.abs(got[bad].view(np.int32).astype(np.int64) -
+                          want[bad].view(np.int32).astype(np.int64))
+            assert ulps.max() <= 1
+
+
+def test_rope_cos_sin_on_all_kernel_angles(lib):
+    # every frequency of head_dim 128 at theta 1e4 and 5e5, positions sampled over [0, 2^20)
+    # and near 2^24: angle = fp32(fp32(pos) * fp32(theta^(-2i/128)))
+    for theta in (10000.0, 500000.0):
+        inv = oracle.rope_inv_freq(theta, 128)
+        pos = np.concatenate([np.arange(0, 1 << 20, 37), np.arange((1 << 24) - 4096, 1 << 24, 3)])
+        ang = (pos.astype(np.float32)[:, None] * inv[None, :]).astype(np.float32).ravel()
+        _check_rounded(ang, f"theta={theta}")
+
+
+def test_rope_cos_sin_random_fp32(lib):
+    g = np.random.Generator(np.random.PCG64(7))
+    e = g.uniform(-30, 24, size=1 << 21)
+    x = (np.sign(g.uniform(-1, 1, size=e.size)) * 2.0 ** e).astype(np.float32)
+    x = x[np.abs(x) < 2 ** 24]
+    _check_rounded(x, "random")
+    # special values and neighbours of multiples of pi/2
+    k = np.arange(-2000, 2000, dtype=np.float64)
+    near = (k * np.pi / 2).astype(np.float32)
+    near = np.concatenate([near, np.nextafter(near, np.float32(np.inf)),
+                           np.nextafter(near, np.float32(-np.inf)),
+                           np.array([0.0, -0.0, 1e-30, -1e-30, 0.5, 1.0], np.float32)])
+    _check_rounded(near.astype(np.float32), "near k*pi/2")
+    c, s = rsn.beam_rope_cos_sin(np.array([0.0, -0.0], np.float32))
+    assert np.all(c == 1.0) and s[0] == 0.0 and np.signbit(s[1])
+
+
+def test_rope_cos_sin_rejects_out_of_range(lib):
+    with pytest.raises(rsn.BeamError):
+        rsn.beam_rope_cos_sin(np.array([2.0 ** 24], np.float32))
+    with pytest.raises(rsn.BeamError):
+        rsn.beam_rope_cos_sin(np.array([np.nan], np.float32))

@@ -1,0 +1,173 @@
+"""GPU parity of the attention-side kernels against the CPU oracle (needs a GB300).
+
+Per-head Q/K RMSNorm + RoPE (sliding-window layers) or + SSMax (NoPE layers), and the sigmoid
+output gate ("Serving Reflection Beam auf vLLM ab Tag 0", section "Attention"; "SGLang 支撑编程模型
+Beam 生产部署", "混合注意力与输出门控").  Decode (T = 128, positions U[0, 2^20)) and an 8 x 2048
+prefill chunk at ~100K context (T = 2048, contiguous positions).
+"""
+import numpy as np
+import pytest
+import torch
+
+import beam_inputs as bi
+import oracle
+import residual_stream_norm_gb300 as rsn
+from tests._gpu import Guarded, dev, lib, u16
+from tests._util import assert_bf16_close
+
+pytestmark = pytest.mark.gpu
+D = bi.HEAD_DIM
+
+
+def run_qk(kind, c, q=None, k=None, **kw):
+    q = dev(c["q"]) if q is None else q
+    k = dev(c["k"]) if k is None else k
+    fn = rsn.beam_qk_norm_rope_fwd if kind == "rope" else rsn.beam_qk_norm_ssmax_fwd
+    fn(q, k, dev(c["wq"]), dev(c["wk"]), dev(c["pos"]), **kw)
+    torch.cuda.synchronize()
+    return q, k
+
+
+def oracle_qk(kind, c, **kw):
+    fn = oracle.qk_norm_rope if kind == "rope" else oracle.qk_norm_ssmax
+    return fn(u16(c["q"]), u16(c["k"]), u16(c["wq"]), u16(c["wk"]), c["pos"].numpy(), **kw)
+
+
+@pytest.mark.parametrize("kind", ["rope", "ssmax"])
+@pytest.mark.parametrize("T,mode", [(128, "uniform"), (2048, "contiguous")])
+def test_attention_side_config(kind, T, mode):
+    lib()
+    c = bi.attn_qk_case(T=T, seed=T, pos_mode=mode)
+    q, k = run_qk(kind, c)
+    wq, wk = oracle_qk(kind, c)
+    assert_bf16_close(u16(q), wq, what=f"{kind} q T={T}")
+    assert_bf16_close(u16(k), wk, what=f"{kind} k T={T}")
+
+
+@pytest.mark.parametrize("kind", ["rope", "ssmax"])
+@pytest.mark.parametrize("nq,nk", [(1, 0), (0, 1), (3, 2), (64, 8), (100, 3)])
+def test_head_counts(kind, nq, nk):
+    c = bi.attn_qk_case(T=5, n_q=nq, n_kv=nk, seed=nq * 10 + nk)
+    q = dev(c["q"]) if nq else torch.empty((5, 0, D), dtype=torch.bfloat16, device="cuda")
+    k = dev(c["k"]) if nk else torch.empty((5, 0, D), dtype=torch.bfloat16, device="cuda")
+    q, k = run_qk(kind, c, q=q, k=k)
+    wq, wk = oracle_qk(kind, c)
+    assert_bf16_close(u16(q), wq, what=f"{kind} q {nq}/{nk}")
+    assert_bf16_close(u16(k), wk, what=f"{kind} k {nq}/{nk}")
+
+
+@pytest.mark.parametrize("kind", ["rope", "ssmax"])
+def test_views_into_packed_qkv_gate_projection(kind):
+    # One packed [T, (48 + 8 + 8) * 128 + 48 * 128] projection output (Q | K | V | gate):
+    # Q and K are row-strided views; V and the gate columns must stay untouched.
+    T = 37
+    c = bi.attn_qk_case(T=T, seed=21)
+    g = bi.rng(22)
+    v = bi.to_bf16(bi.normal(g, (T, 8 * D)))
+    gate = bi.to_bf16(bi.normal(g, (T, 48 * D)))
+    packed = torch.cat([c["q"].reshape(T, -1), c["k"].reshape(T, -1), v, gate], dim=1)
+    buf = Guarded(tuple(packed.shape), fill=dev(packed))
+    qv = buf.view[:, : 48 * D].view(T, 48, D)
+    kv = buf.view[:, 48 * D: 56 * D].view(T, 8, D)
+    run_qk(kind, c, q=qv, k=kv)
+    buf.check()
+    wq, wk = oracle_qk(kind, c)
+    assert_bf16_close(u16(qv.contiguous()), wq, what="strided q")
+    assert_bf16_close(u16(kv.contiguous()), wk, what="strided k")
+    assert torch.equal(buf.view[:, 56 * D:].cpu(), torch.cat([v, gate], dim=1))
+
+
+def test_rope_theta_and_special_positions():
+    c = bi.attn_qk_case(T=8, seed=23)
+    c["pos"] = torch.tensor([0, 1, 2, 511, 4095, 98_304, (1 << 20) - 1, (1 << 24) - 1],
+                            dtype=torch.int64)
+    for theta in (10000.0, 1e6):
+        q, k = run_qk("rope", c, theta=theta)
+        wq, wk = oracle_qk("rope", c, theta=theta)
+        assert_bf16_close(u16(q), wq, what=f"rope theta={theta}")
+        assert_bf16_close(u16(k), wk, what=f"rope theta={theta}")
+
+
+def test_ssmax_parameters_and_positions():
+    c = bi.attn_qk_case(T=6, seed=24)
+    c["pos"] = torch.tensor([0, 63487, 2095103, 7, 1 << 20, 123456], dtype=torch.int64)
+    for base, ex in ((2048.0, 0.1), (512.0, 0.25)):
+        q, k = run_qk("ssmax", c, ssmax_base=base, ssmax_exp=ex)
+        wq, wk = oracle_qk("ssmax", c, base=base, expo=ex)
+        assert_bf16_close(u16(q), wq, what=f"ssmax base={base}")
+        assert_bf16_close(u16(k), wk, what=f"ssmax base={base}")
+
+
+# ------------------------------------------------------------------------------------------
+# gate
+# ------------------------------------------------------------------------------------------
+
+def run_gate(c, out=None, nh=bi.N_Q_HEADS, hd=D):
+    attn = dev(c["attn"])
+    out = torch.empty_like(attn) if out is None else out
+    rsn.beam_attn_gate_fwd(out, attn, dev(c["gate"]), dev(c["bias"]), nh, hd)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_gate(c, nh=bi.N_Q_HEADS, hd=D):
+    return oracle.attn_gate(u16(c["attn"]), u16(c["gate"]), c["bias"].numpy(), nh, hd)
+
+
+@pytest.mark.parametrize("T", [128, 2048])
+def test_gate_config(T):
+    c = bi.gate_case(T=T, seed=T)
+    assert_bf16_close(u16(run_gate(c)), oracle_gate(c), what=f"gate T={T}")
+
+
+@pytest.mark.parametrize("nh,hd", [(1, 8), (3, 16), (48, 128), (7, 1024), (1024, 8)])
+def test_gate_shapes(nh, hd):
+    c = bi.gate_case(T=9, n_heads=nh, D=hd, seed=nh + hd)
+    assert_bf16_close(u16(run_gate(c, nh=nh, hd=hd)), oracle_gate(c, nh, hd),
+                      what=f"gate {nh}x{hd}")
+
+
+def test_gate_switch_off_pass_through_and_in_place():
+    c = bi.gate_case(T=17, seed=31)
+    bias = c["bias"].clone()
+    bias[0] = -float("inf")
+    bias[1] = float("inf")
+    c2 = dict(c, bias=bias)
+    attn = dev(c["attn"])
+    rsn.beam_attn_gate_fwd(attn, attn, dev(c["gate"]), dev(bias), bi.N_Q_HEADS, D)  # in place
+    torch.cuda.synchronize()
+    got = u16(attn)
+    assert_bf16_close(got, oracle_gate(c2), what="gate in place")
+    heads = got.reshape(17, bi.N_Q_HEADS, D)
+    assert np.all((heads[:, 0] & 0x7FFF) == 0)                      # switched off
+    assert np.array_equal(heads[:, 1], u16(c["attn"]).reshape(17, bi.N_Q_HEADS, D)[:, 1])
+
+
+def test_gate_strided_rows_and_guards():
+    T = 11
+    c = bi.gate_case(T=T, seed=32)
+    C = bi.N_Q_HEADS * D
+    big = Guarded((T, C + 64), fill=dev(torch.cat([c["attn"], torch.zeros(T, 64,
+                                                                         dtype=torch.bfloat16)],
+                                                        dim=1)))
+    gbuf = dev(torch.cat([c["gate"], torch.zeros(T, 128, dtype=torch.bfloat16)], dim=1))
+    out = Guarded((T, C + 8))
+    rsn.beam_attn_gate_fwd(out.view[:, :C], big.view[:, :C], gbuf[:, :C], dev(c["bias"]),
+                           bi.N_Q_HEADS, D)
+    torch.cuda.synchronize()
+    big.check()
+    out.check()
+    assert_bf16_close(u16(out.view[:, :C].contiguous()), oracle_gate(c), what="strided gate")
+    assert bool((out.view[:, C:] == -12345.0).all())
+
+
+def test_zero_tokens():
+    q = torch.empty((0, 48, D), dtype=torch.bfloat16, device="cuda")
+    k = torch.empty((0, 8, D), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(D, dtype=torch.bfloat16, device="cuda")
+    pos = torch.empty((0,), dtype=torch.int64, device="cuda")
+    rsn.beam_qk_norm_rope_fwd(q, k, w, w, pos)
+    rsn.beam_qk_norm_ssmax_fwd(q, k, w, w, pos)
+    a = torch.empty((0, 48 * D), dtype=torch.bfloat16, device="cuda")
+    rsn.beam_attn_gate_fwd(a, a, a, torch.zeros(48, device="cuda"), 48, D)
+    torch.cuda.synchronize()
