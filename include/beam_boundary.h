@@ -64,6 +64,14 @@ BEAM_API const char *beam_status_str(int status);
  * Returns BEAM_ERR_INVALID_ARG for n < 1 or NULL outputs. */
 BEAM_API int beam_residual_scales(int32_t n, float *alpha, float *s);
 
+/* Host-only helper: the FP32 quotient x / s (s = fp32(sqrt(n))) exactly as the boundary kernels
+ * form it before rounding b = bf16(x / s): for n <= 4096 and 2^-99 <= |x| < inf by Markstein's
+ * FMA correction step (y = RN(1/s), q = RN(x y), q' = RN(q + (x - q s) y)), otherwise by IEEE
+ * division; the result equals IEEE division for every finite BF16 x (checked exhaustively by the
+ * tests).  `count` values in host memory.  Returns BEAM_ERR_INVALID_ARG for n < 1, count < 0 or
+ * NULL arrays. */
+BEAM_API int beam_residual_quotient(const float *x, float *q_out, int64_t count, int32_t n);
+
 /* Host-only helper: the FP32 cosine and sine that beam_qk_norm_rope_fwd uses for an FP32 rotary
  * angle, for `count` angles in host memory.  Each value is the FP32 rounding of the exact
  * cos / sin of the FP32 angle (except in rare near-tie cases), computed in FP32 pair arithmetic

@@ -19,7 +19,8 @@ import torch
 from . import _build
 
 __all__ = ["BeamError", "build", "lib", "beam_abi_version", "beam_status_str",
-           "beam_residual_scales", "beam_rope_cos_sin", "beam_boundary_fwd", "beam_moe_combine_boundary_fwd",
+           "beam_residual_scales", "beam_rope_cos_sin", "beam_residual_quotient",
+           "beam_boundary_fwd", "beam_moe_combine_boundary_fwd",
            "beam_qk_norm_rope_fwd", "beam_qk_norm_ssmax_fwd", "beam_attn_gate_fwd",
            "HEAD_DIM"]
 
@@ -56,6 +57,7 @@ def lib() -> ctypes.CDLL:
             so.beam_status_str.restype = ctypes.c_char_p
             so.beam_residual_scales.argtypes = [i32, ctypes.POINTER(f32), ctypes.POINTER(f32)]
             so.beam_rope_cos_sin.argtypes = [vp, vp, vp, i64]
+            so.beam_residual_quotient.argtypes = [vp, vp, i64, i32]
             so.beam_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, f32, vp, vp]
             so.beam_moe_combine_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, i64,
                                                          i32, i32, i32, f32, vp, vp]
@@ -65,6 +67,7 @@ def lib() -> ctypes.CDLL:
                                                   i32, f32, f32, f32, vp]
             so.beam_attn_gate_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i64, vp]
             for fn in ("beam_abi_version", "beam_residual_scales", "beam_rope_cos_sin",
+                       "beam_residual_quotient",
                        "beam_boundary_fwd",
                        "beam_moe_combine_boundary_fwd", "beam_qk_norm_rope_fwd",
                        "beam_qk_norm_ssmax_fwd", "beam_attn_gate_fwd"):
@@ -124,6 +127,17 @@ def beam_residual_scales(n: int) -> tuple[float, float]:
     if st != 0:
         raise BeamError("beam_residual_scales", st)
     return a.value, s.value
+
+
+def beam_residual_quotient(x, n: int):
+    """Host helper: the FP32 quotient x / fp32(sqrt(n)) exactly as the boundary kernels form it."""
+    import numpy as np
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    q = np.empty_like(a)
+    st = lib().beam_residual_quotient(a.ctypes.data, q.ctypes.data, a.size, n)
+    if st != 0:
+        raise BeamError("beam_residual_quotient", st)
+    return q
 
 
 def beam_rope_cos_sin(angle):

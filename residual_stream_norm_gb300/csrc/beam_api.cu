@@ -10,6 +10,7 @@
 
 #include "../../include/beam_boundary.h"
 #include "beam_kernels.h"
+#include "beam_f32x2.cuh"
 #include "beam_sincos.cuh"
 
 namespace {
@@ -86,6 +87,18 @@ int beam_residual_scales(int32_t n, float *alpha, float *s)
         return BEAM_ERR_INVALID_ARG;
     *alpha = (float)std::sqrt((double)(n - 1) / (double)n);
     *s = (float)std::sqrt((double)n);
+    return BEAM_OK;
+}
+
+int beam_residual_quotient(const float *x, float *q_out, int64_t count, int32_t n)
+{
+    if (n < 1 || count < 0 || (count > 0 && (!x || !q_out)))
+        return BEAM_ERR_INVALID_ARG;
+    float alpha, s;
+    beam_residual_scales(n, &alpha, &s);
+    const float y = 1.0f / s;
+    for (int64_t i = 0; i < count; ++i)
+        q_out[i] = beam::residual_quotient_host(x[i], n, s, y);
     return BEAM_OK;
 }
 

@@ -36,7 +36,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 9, names
+    assert len(names) == 10, names
     raw = ctypes.CDLL(rsn.LIB_PATH)
     for nm in names:
         assert hasattr(raw, nm), f"{nm} declared in the header but not exported"
@@ -189,3 +189,27 @@ def test_rope_cos_sin_rejects_out_of_range(lib):
         rsn.beam_rope_cos_sin(np.array([2.0 ** 24], np.float32))
     with pytest.raises(rsn.BeamError):
         rsn.beam_rope_cos_sin(np.array([np.nan], np.float32))
+
+
+# ------------------------------------------------------------------------------------------
+# the residual operand division (host build of the kernels' arithmetic)
+# ------------------------------------------------------------------------------------------
+
+def test_residual_quotient_equals_ieee_division_exhaustively(lib):
+    # every finite BF16 value x (subnormals and signed zeros included) and every residual index
+    # n = 1..4096: the kernels' x / s must be the IEEE (correctly rounded) FP32 quotient.
+    b = np.arange(1 << 16, dtype=np.uint32)
+    x = (b << 16).view(np.float32)
+    x = x[np.isfinite(x)]
+    for n in range(1, 4097):
+        s = np.float32(np.sqrt(np.float64(n)))
+        q = rsn.beam_residual_quotient(x, n)
+        assert np.array_equal(q.view(np.uint32), (x / s).view(np.uint32)), n
+
+
+def test_residual_quotient_large_n_and_nonfinite(lib):
+    x = np.array([1.0, -3.5, 1e-30, 7e37, np.inf, -np.inf], dtype=np.float32)
+    for n in (3, 4097, 10**6, 2**31 - 1):
+        s = np.float32(np.sqrt(np.float64(n)))
+        assert np.array_equal(rsn.beam_residual_quotient(x, n), x / s)
+    assert np.isnan(rsn.beam_residual_quotient(np.array([np.nan], np.float32), 5)).all()
