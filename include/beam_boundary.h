@@ -64,6 +64,13 @@ BEAM_API const char *beam_status_str(int status);
  * Returns BEAM_ERR_INVALID_ARG for n < 1 or NULL outputs. */
 BEAM_API int beam_residual_scales(int32_t n, float *alpha, float *s);
 
+/* Fault word of the current device.  The persistent kernels wait on their own bulk copies with a
+ * time limit (2 s); a kernel that gives up drains its copies, sets bit 0 (1 = copy wait timed
+ * out) and returns without writing the rest of its rows.  Never set in normal operation.
+ * Synchronous (a device-to-host copy on the legacy default stream); `clear` != 0 resets the word.
+ * No counterpart on the pages: a diagnostic of this library. */
+BEAM_API int beam_device_faults(uint32_t *flags, int clear);
+
 /* Host-only helper: the FP32 quotient x / s (s = fp32(sqrt(n))) exactly as the boundary kernels
  * form it before rounding b = bf16(x / s): for n <= 4096 and 2^-99 <= |x| < inf by Markstein's
  * FMA correction step (y = RN(1/s), q = RN(x y), q' = RN(q + (x - q s) y)), otherwise by IEEE

@@ -19,7 +19,7 @@ import torch
 from . import _build
 
 __all__ = ["BeamError", "build", "lib", "beam_abi_version", "beam_status_str",
-           "beam_residual_scales", "beam_rope_cos_sin", "beam_residual_quotient",
+           "beam_residual_scales", "beam_rope_cos_sin", "beam_residual_quotient", "beam_device_faults",
            "beam_boundary_fwd", "beam_moe_combine_boundary_fwd",
            "beam_qk_norm_rope_fwd", "beam_qk_norm_ssmax_fwd", "beam_attn_gate_fwd",
            "HEAD_DIM"]
@@ -58,6 +58,7 @@ def lib() -> ctypes.CDLL:
             so.beam_residual_scales.argtypes = [i32, ctypes.POINTER(f32), ctypes.POINTER(f32)]
             so.beam_rope_cos_sin.argtypes = [vp, vp, vp, i64]
             so.beam_residual_quotient.argtypes = [vp, vp, i64, i32]
+            so.beam_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
             so.beam_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, f32, vp, vp]
             so.beam_moe_combine_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, i64,
                                                          i32, i32, i32, f32, vp, vp]
@@ -67,7 +68,7 @@ def lib() -> ctypes.CDLL:
                                                   i32, f32, f32, f32, vp]
             so.beam_attn_gate_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i64, vp]
             for fn in ("beam_abi_version", "beam_residual_scales", "beam_rope_cos_sin",
-                       "beam_residual_quotient",
+                       "beam_residual_quotient", "beam_device_faults",
                        "beam_boundary_fwd",
                        "beam_moe_combine_boundary_fwd", "beam_qk_norm_rope_fwd",
                        "beam_qk_norm_ssmax_fwd", "beam_attn_gate_fwd"):
@@ -127,6 +128,16 @@ def beam_residual_scales(n: int) -> tuple[float, float]:
     if st != 0:
         raise BeamError("beam_residual_scales", st)
     return a.value, s.value
+
+
+def beam_device_faults(clear: bool = False) -> int:
+    """The device fault word (0 in normal operation; bit 0: a kernel gave up waiting for its own
+    bulk copies).  Synchronous."""
+    v = ctypes.c_uint32()
+    st = lib().beam_device_faults(ctypes.byref(v), int(clear))
+    if st != 0:
+        raise BeamError("beam_device_faults", st)
+    return v.value
 
 
 def beam_residual_quotient(x, n: int):

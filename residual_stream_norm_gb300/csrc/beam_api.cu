@@ -90,6 +90,16 @@ int beam_residual_scales(int32_t n, float *alpha, float *s)
     return BEAM_OK;
 }
 
+int beam_device_faults(uint32_t *flags, int clear)
+{
+    if (!flags)
+        return BEAM_ERR_INVALID_ARG;
+    unsigned int v = 0u;
+    const cudaError_t e = beam::read_fault_word(&v, clear != 0);
+    *flags = v;
+    return cuda_status(e);
+}
+
 int beam_residual_quotient(const float *x, float *q_out, int64_t count, int32_t n)
 {
     if (n < 1 || count < 0 || (count > 0 && (!x || !q_out)))
@@ -145,6 +155,8 @@ int beam_boundary_fwd(void *h_out, void *y_out, const void *h_in, const void *x_
     a.K = 0;
     a.eps = eps;
     beam_residual_scales(n, &a.alpha, &a.s);
+    a.inv_s = 1.0f / a.s;
+    a.fast_div_n = n <= beam::kMarksteinMaxN;
     return cuda_status(beam::launch_boundary(a, stream));
 }
 
@@ -180,6 +192,8 @@ int beam_moe_combine_boundary_fwd(void *h_out, void *y_out, const void *h_in,
     a.K = K;
     a.eps = eps;
     beam_residual_scales(n, &a.alpha, &a.s);
+    a.inv_s = 1.0f / a.s;
+    a.fast_div_n = n <= beam::kMarksteinMaxN;
     return cuda_status(beam::launch_moe_boundary(a, stream));
 }
 

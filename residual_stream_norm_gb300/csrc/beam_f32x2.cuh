@@ -75,19 +75,9 @@ __device__ __forceinline__ f2 make_f2(float lo, float hi)
 
 __device__ __forceinline__ f2 splat(float v) { return make_f2(v, v); }
 
-__device__ __forceinline__ float lo_of(f2 v)
-{
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return lo;
-}
+__device__ __forceinline__ float lo_of(f2 v) { return __uint_as_float((uint32_t)v); }
 
-__device__ __forceinline__ float hi_of(f2 v)
-{
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-    return hi;
-}
+__device__ __forceinline__ float hi_of(f2 v) { return __uint_as_float((uint32_t)(v >> 32)); }
 
 __device__ __forceinline__ f2 add2(f2 a, f2 b)
 {

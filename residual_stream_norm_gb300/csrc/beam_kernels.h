@@ -23,6 +23,8 @@ struct BoundaryArgs {
     float routed_scaling;
     float alpha;             // fp32(sqrt((n-1)/n))
     float s;                 // fp32(sqrt(n))
+    float inv_s;             // fp32(1 / s), IEEE division on the host
+    bool fast_div_n;         // n small enough for the Markstein division step
     float eps;
 };
 
@@ -63,5 +65,9 @@ cudaError_t launch_moe_boundary(const BoundaryArgs &a, cudaStream_t stream);
 cudaError_t launch_qk_norm_rope(const QkArgs &a, cudaStream_t stream);
 cudaError_t launch_qk_norm_ssmax(const QkArgs &a, cudaStream_t stream);
 cudaError_t launch_attn_gate(const GateArgs &a, cudaStream_t stream);
+
+// The device fault word of the current device (bit 0: a kernel gave up waiting for its own bulk
+// copies); synchronous.
+cudaError_t read_fault_word(unsigned int *value, bool clear);
 
 }  // namespace beam

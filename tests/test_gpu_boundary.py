@@ -49,6 +49,9 @@ def test_single_boundary_config():
 @pytest.mark.parametrize("T,H,n", [
     (1, 8, 1), (3, 16, 2), (2, 24, 3), (37, 5120, 7), (5, 5128, 104), (3, 16384, 11),
     (300, 5120, 9), (307, 4104, 50), (64, 16384, 1), (40, 5120, 1_000_000),
+    # enough rows for the persistent TMA ring (>= 4 rows per SM), ragged and maximum H
+    (700, 5120, 13), (613, 5128, 2), (1000, 16384, 104), (2000, 8, 3), (640, 24, 77),
+    (650, 5120, 5000),
 ])
 def test_shapes(T, H, n):
     c = bi.boundary_case(T=T, H=H, n=n, seed=T + H, outlier_frac=0.05, outlier_mult=16.0,
@@ -186,3 +189,23 @@ def test_eps_zero_and_large():
         want = oracle.boundary(u16(c["h"]), u16(c["x"]), u16(c["w_post"]), u16(c["w_pre"]), 2,
                                eps)
         check(got, want, f"eps={eps}")
+
+
+def test_huge_weights_take_the_ieee_division_path():
+    # |w_post| >= 2^120 can overflow x_hat to inf; those threads must divide by IEEE division.
+    for T in (5, 700):
+        c = bi.boundary_case(T=T, n=3, seed=12)
+        w = u16(c["w_post"]).copy()
+        w[::97] = 0x7E80  # 2^122
+        w[5] = 0x7F7F     # largest finite BF16
+        wb = bi.from_u16(w)
+        got = run_gpu(c["h"], c["x"], wb, c["w_pre"], 3)
+        want = oracle.boundary(u16(c["h"]), u16(c["x"]), w, u16(c["w_pre"]), 3)
+        assert_bf16_close(got[0], want[0], min_equal=0.99, what=f"huge w T={T} h'")
+        assert_bf16_close(got[1], want[1], min_equal=0.99, what=f"huge w T={T} y")
+
+
+def test_no_device_faults_raised():
+    # The persistent kernels bound every wait on their own copies; none may have given up.
+    torch.cuda.synchronize()
+    assert rsn.beam_device_faults() == 0

@@ -61,7 +61,11 @@ def test_decode_moe_boundaries_layers_3_to_51():
 
 
 @pytest.mark.parametrize("T,H,K", [(1, 8, 1), (3, 16, 3), (5, 5120, 16), (2, 5128, 8),
-                                   (310, 5120, 8), (4, 16384, 8), (300, 16384, 2)])
+                                   (310, 5120, 8), (4, 16384, 8), (300, 16384, 2),
+                                   # persistent TMA ring (>= 4 rows per SM), and shapes whose
+                                   # stages do not fit shared memory (per-row fallback)
+                                   (700, 5120, 8), (650, 5128, 1), (620, 16384, 2),
+                                   (610, 5120, 16), (900, 16384, 8), (1500, 8, 8)])
 def test_shapes(T, H, K):
     c = bi.moe_case(T=T, H=H, K=K, seed=T * 7 + K)
     check(run_gpu(c["h"], c["e"], c["topk_w"], c["w_post"], c["w_pre"], c["n"]), oracle_run(c),
