@@ -79,6 +79,12 @@ def barrier(ws: int):
         torch.distributed.barrier()
 
 
+def whole_job_rate(ws: int, tokens_per_rank: int, steps: int, max_ms: float) -> float:
+    """Tokens per second of the whole job: every rank processed its own batch each step, and the
+    job took as long as its slowest rank."""
+    return ws * tokens_per_rank * steps / (max_ms * 1e-3)
+
+
 def max_over_ranks(x: float, ws: int, device) -> float:
     if ws == 1:
         return x
@@ -405,7 +411,7 @@ def run_gpu_arm(args) -> None:
                      / args.steps for j in range(nk)}
     max_ms = max_over_ranks(total_ms, ws, device)
     T = step.T
-    value = ws * T * args.steps / (max_ms * 1e-3)
+    value = whole_job_rate(ws, T, args.steps, max_ms)
 
     peak, peak_src = measured_peak()
     kernels = {}
