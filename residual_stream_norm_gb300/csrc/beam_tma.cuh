@@ -50,6 +50,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         : "memory");
 }
 
+// Plain arrive (release semantics) on `bar`.
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Barrier among the first `count` threads of the CTA only (named barrier `id`, id >= 1).
+__device__ __forceinline__ void named_sync(int id, int count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
@@ -68,6 +80,26 @@ __device__ __forceinline__ unsigned long long global_ns()
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// Wait for phase `parity` of `bar`, giving up when the CTA's shared `fail` flag is set (some
+// thread already gave up) or after kWaitLimitNs (then this thread sets `fail`).  False when it
+// gave up.
+__device__ __forceinline__ bool mbar_wait_or_fail(uint64_t *bar, uint32_t parity,
+                                                  volatile int *fail)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*fail)
+            return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            *fail = 1;
+            return false;
+        }
+    }
+    return true;
 }
 
 // Wait for phase `parity` of `bar` to complete; false if it did not within kWaitLimitNs.

@@ -15,12 +15,13 @@
 // Two layouts, same arithmetic (boundary_chain):
 //  * rows kernel (few tokens, e.g. batch-1 decode): one CTA per token row; each thread owns VPT
 //    16-byte vectors at vector indices tid + i * blockDim.x and loads them straight from memory.
-//  * ring kernel (many tokens): a persistent grid (SM count x CTAs per SM) in which each CTA
-//    walks its rows through a ring of shared-memory stages.  One thread issues bulk TMA copies
-//    (cp.async.bulk, completion on an mbarrier) of the next rows' inputs -- the x row or the K
-//    expert rows, and the h row -- so several rows' copies are in flight while the current row
-//    is reduced; a stage is refilled as soon as the first block reduction shows that every
-//    thread has read it.  Each thread keeps its slice of both norm weights in registers.
+//  * ring kernel (many tokens): a persistent grid (SM count x CTAs per SM) with warp
+//    specialisation: one producer warp issues bulk TMA copies (cp.async.bulk, completion on
+//    "full" mbarriers) of each row's inputs in chunks of 128 vectors -- the x chunk or the K
+//    expert chunks, and the h chunk -- into a ring of shared-memory stages, and four consumer
+//    warps reduce and finish the rows, releasing each stage on an "empty" mbarrier as soon as
+//    they have read it.  Only 4 warps share a row, so the two block reductions per row stay
+//    cheap, and several CTAs fit on an SM.
 // The row stays in registers as packed BF16 between the two block reductions; element math runs
 // on packed FP32 pairs (beam_f32x2.cuh) with the same IEEE roundings as the scalar definition.
 
@@ -40,18 +41,34 @@ namespace {
 
 constexpr int kMaxK = 16;
 
-// Block-wide sum; every warp combines the per-warp partials with the same butterfly, so all
-// threads get identical bits.  `slot` holds >= 32 entries not used by a concurrent reduction.
-__device__ __forceinline__ float block_sum_w(Sum2 a, Sum2 *slot)
+// Block-wide sum over `nt` threads (a multiple of 32).  `named`: synchronise only those
+// threads on named barrier 1 (the ring kernel's consumer warps); otherwise __syncthreads.
+// Warp partials go through `slot` (>= 32 entries no concurrent reduction uses); every warp
+// combines them with the same butterfly, so all threads get identical bits.
+__device__ __forceinline__ float block_sum_w(Sum2 a, Sum2 *slot, int nt, bool named)
 {
     a = warp_sum(a);
     const int lane = threadIdx.x & 31;
-    const int nw = blockDim.x >> 5;
+    const int nw = nt >> 5;
     if (lane == 0)
         slot[threadIdx.x >> 5] = a;
-    __syncthreads();
-    const Sum2 p = lane < nw ? slot[lane] : Sum2{0.0f, 0.0f};
-    return sum_value(warp_sum(p));
+    if (named)
+        named_sync(1, nt);
+    else
+        __syncthreads();
+    Sum2 p = lane < nw ? slot[lane] : Sum2{0.0f, 0.0f};
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        if (off < nw) {
+            Sum2 o;
+            o.hi = __shfl_xor_sync(0xffffffffu, p.hi, off);
+            o.lo = __shfl_xor_sync(0xffffffffu, p.lo, off);
+            p = sum_merge(p, o);
+        }
+    }
+    p.hi = __shfl_sync(0xffffffffu, p.hi, 0);
+    p.lo = __shfl_sync(0xffffffffu, p.lo, 0);
+    return sum_value(p);
 }
 
 __device__ __forceinline__ Sum2 lanes_merged(const Sum2x2 &a)
@@ -59,35 +76,34 @@ __device__ __forceinline__ Sum2 lanes_merged(const Sum2x2 &a)
     return sum_merge(Sum2{lo_of(a.hi), lo_of(a.lo)}, Sum2{hi_of(a.hi), hi_of(a.lo)});
 }
 
-// True when every BF16 element of this thread's post-norm weight slice has |w| < 2^120, so
-// xhat = bf16((x r) w) cannot overflow and the Markstein division step is safe for it.
-template <int VPT>
-__device__ __forceinline__ bool weights_small(const uint4 (&w)[VPT])
+// True when every BF16 element in `w` has |w| < 2^120, so that xhat = bf16((x r) w) cannot
+// overflow and the Markstein division step is safe for it.
+template <int N>
+__device__ __forceinline__ bool weights_small(const uint4 (&w)[N])
 {
     constexpr uint32_t kCeil = (kWeightMaxExp << 7) | (kWeightMaxExp << 23);
     uint32_t any = 0u;
 #pragma unroll
-    for (int i = 0; i < VPT; ++i)
+    for (int i = 0; i < N; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             any |= ((word(w[i], j) & 0x7f807f80u) | 0x80008000u) - kCeil;
     return (any & 0x80008000u) == 0u;
 }
 
-// The boundary chain for one row whose inputs sit in registers (xv: x, hv: h; wpo / wpr: this
-// thread's slices of the weights).  `after_first_sum` runs right after the first block
-// reduction (the ring kernel refills its stage there).  `fast_div`: the thread may use the
-// Markstein step for x_hat / s (n small enough and its weights small).
-template <int VPT, typename AfterFirstSum>
+// The boundary chain for one row whose inputs sit in registers: xv (x) and hv (h) hold this
+// thread's vectors tid + i * nt.  wpo(i) / wpr(i) give the matching weight vectors.
+// `after_first_sum` runs right after the first block reduction.  `fast_div`: this thread may
+// use the Markstein step for x_hat / s (n small enough and its weights small).
+template <int VPT, typename WPost, typename WPre, typename AfterFirstSum>
 __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t row,
                                                const uint4 (&xv)[VPT], const uint4 (&hv)[VPT],
-                                               const uint4 (&wpo)[VPT], const uint4 (&wpr)[VPT],
-                                               bool fast_div, Sum2 (*red)[32],
+                                               WPost wpo, WPre wpr, bool fast_div,
+                                               Sum2 (*red)[32], int nt, bool named,
                                                AfterFirstSum after_first_sum)
 {
     const int nvec = a.H >> 3;
     const int tid = threadIdx.x;
-    const int nt = blockDim.x;
     const int64_t row_off = row * (int64_t)a.H;
 
     // ---- a1: r = 1/sqrt(mean(x^2) + eps) ---------------------------------------------------
@@ -100,7 +116,7 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
             sum2_add(acc, mul2(x, x));
         }
     }
-    const float r = rms_inv(block_sum_w(lanes_merged(acc), red[0]), (float)a.H, a.eps);
+    const float r = rms_inv(block_sum_w(lanes_merged(acc), red[0], nt, named), (float)a.H, a.eps);
     after_first_sum();
 
     // ---- a1 / a2: xhat = bf16((x r) w_post); h' = bf16(bf16(alpha h) + bf16(xhat / s)) -----
@@ -112,11 +128,12 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
         const int v = tid + i * nt;
         hp[i] = make_uint4(0u, 0u, 0u, 0u);
         if (v < nvec) {
+            const uint4 w = wpo(i);
             uint32_t xh[4], bw[4];
             uint32_t floor_all = 0xffffffffu;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                xh[j] = narrow(mul2(mul2(widen(word(xv[i], j)), rr), widen(word(wpo[i], j))));
+                xh[j] = narrow(mul2(mul2(widen(word(xv[i], j)), rr), widen(word(w, j))));
                 exp_floor_check(floor_all, xh[j]);
             }
             if (fast_div && exp_floor_ok(floor_all)) {
@@ -140,7 +157,8 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
             }
         }
     }
-    const f2 rr2 = splat(rms_inv(block_sum_w(lanes_merged(acc), red[1]), (float)a.H, a.eps));
+    const f2 rr2 =
+        splat(rms_inv(block_sum_w(lanes_merged(acc), red[1], nt, named), (float)a.H, a.eps));
 
     // ---- a3: y = bf16((h' r') w_pre); store h' and y -----------------------------------------
     char *h_out = (char *)a.h_out + 2 * row_off;
@@ -149,10 +167,11 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
     for (int i = 0; i < VPT; ++i) {
         const int v = tid + i * nt;
         if (v < nvec) {
+            const uint4 w = wpr(i);
             uint4 yv;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                word(yv, j) = narrow(mul2(mul2(widen(word(hp[i], j)), rr2), widen(word(wpr[i], j))));
+                word(yv, j) = narrow(mul2(mul2(widen(word(hp[i], j)), rr2), widen(word(w, j))));
             st_global(h_out + 16 * (int64_t)v, hp[i]);
             st_global(y_out + 16 * (int64_t)v, yv);
         }
@@ -186,17 +205,17 @@ __device__ __forceinline__ uint4 combine_vec(const float (&c)[kMaxK], int K,
     return x;
 }
 
-template <int VPT>
-__device__ __forceinline__ void load_weights(const BoundaryArgs &a, uint4 (&wpo)[VPT],
-                                             uint4 (&wpr)[VPT])
+__device__ __forceinline__ uint4 weight_vec(const void *w, int v, int nvec)
 {
-    const int nvec = a.H >> 3;
+    return v < nvec ? ld_cached((const char *)w + 16 * (int64_t)v) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+__device__ __forceinline__ void routing_coeffs(const BoundaryArgs &a, int64_t row,
+                                               float (&c)[kMaxK])
+{
 #pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-        const int v = threadIdx.x + i * blockDim.x;
-        wpo[i] = v < nvec ? ld_cached((const char *)a.w_post + 16 * (int64_t)v) : make_uint4(0u, 0u, 0u, 0u);
-        wpr[i] = v < nvec ? ld_cached((const char *)a.w_pre + 16 * (int64_t)v) : make_uint4(0u, 0u, 0u, 0u);
-    }
+    for (int k = 0; k < kMaxK; ++k)
+        c[k] = k < a.K ? __fmul_rn(a.topk_w[row * a.K + k], a.routed_scaling) : 0.0f;
 }
 
 // ---- rows kernel: one CTA per row, inputs straight from memory ------------------------------
@@ -210,19 +229,20 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
     uint4 wpo[VPT], wpr[VPT];
-    load_weights<VPT>(a, wpo, wpr);
-    const bool fast_div = a.fast_div_n && weights_small<VPT>(wpo);
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+        wpo[i] = weight_vec(a.w_post, tid + i * nt, nvec);
+        wpr[i] = weight_vec(a.w_pre, tid + i * nt, nvec);
+    }
+    const bool fast_div = a.fast_div_n && weights_small(wpo);
 
     for (int64_t row = blockIdx.x; row < a.T; row += gridDim.x) {
         const int64_t row_off = row * (int64_t)a.H;
         const char *h_in = (const char *)a.h_in + 2 * row_off;
         uint4 xv[VPT], hv[VPT];
         float c[kMaxK];
-        if constexpr (MOE) {
-#pragma unroll
-            for (int k = 0; k < kMaxK; ++k)
-                c[k] = k < a.K ? __fmul_rn(a.topk_w[row * a.K + k], a.routed_scaling) : 0.0f;
-        }
+        if constexpr (MOE)
+            routing_coeffs(a, row, c);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int v = tid + i * nt;
@@ -239,102 +259,135 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
                 hv[i] = xv[i];
             }
         }
-        boundary_chain<VPT>(a, row, xv, hv, wpo, wpr, fast_div, red, [] {});
+        boundary_chain<VPT>(
+            a, row, xv, hv, [&](int i) { return wpo[i]; }, [&](int i) { return wpr[i]; },
+            fast_div, red, nt, false, [] {});
     }
 }
 
-// ---- ring kernel: persistent CTAs, TMA bulk copies through shared-memory stages -------------
+// ---- ring kernel: persistent, warp-specialised TMA pipeline ---------------------------------
+//
+// A CTA has NC consumer threads (kRingConsumers, 4 warps) and one producer warp.  Its rows are
+// blockIdx.x, blockIdx.x + gridDim.x, ...; each row is cut into VPT chunks of NC 16-byte
+// vectors, and consumer thread t owns vector c * NC + t of chunk c.  A unit of work is one chunk
+// of one row; its stage holds KIN input slices (the x chunk, or the K expert chunks) and the h
+// chunk, each NC * 16 bytes.  Per stage two mbarriers: `full` completes when the producer's
+// bulk copies have landed (transaction bytes), `empty` when all consumer warps have read the
+// stage (one arrive per warp).  The producer keeps `stages` units in flight.
 
-constexpr int kRingHeader = 128;  // the stages' mbarriers live in the first 128 bytes
+constexpr int kRingConsumers = 128;
+constexpr int kRingHeader = 256;  // 2 x up to 16 mbarriers
+constexpr int kRingMaxStages = 16;
 
 template <int VPT, bool MOE>
-__global__ void __launch_bounds__(VPT == 1 ? 1024 : 512)
-    boundary_ring_kernel(const BoundaryArgs a, int stages, uint32_t stage_bytes)
+__global__ void __launch_bounds__(kRingConsumers + 32)
+    boundary_ring_kernel(const BoundaryArgs a, int stages)
 {
     extern __shared__ __align__(128) unsigned char dyn[];
     uint64_t *full = reinterpret_cast<uint64_t *>(dyn);
+    uint64_t *empty = full + kRingMaxStages;
     unsigned char *ring = dyn + kRingHeader;
     __shared__ Sum2 red[2][32];
+    __shared__ int fail;
 
+    constexpr int NC = kRingConsumers;
+    constexpr uint32_t kSlice = NC * 16;
     const int nvec = a.H >> 3;
     const int tid = threadIdx.x;
-    const int nt = blockDim.x;
-    const uint32_t row_bytes = 2u * (uint32_t)a.H;
-    const int K = MOE ? a.K : 1;
-    const uint32_t in_bytes = (uint32_t)K * row_bytes;  // the x row, or the K expert rows
+    const int KIN = MOE ? a.K : 1;
+    const uint32_t stage_bytes = (uint32_t)(KIN + 1) * kSlice;
     const int64_t first = blockIdx.x;
     const int64_t stride = gridDim.x;
     const int64_t my_rows = first < a.T ? (a.T - first + stride - 1) / stride : 0;
-
-    auto issue = [&](int64_t i) {  // one thread: fill stage i % stages with row i's inputs
-        const int st = (int)(i % stages);
-        const int64_t row = first + i * stride;
-        unsigned char *dst = ring + (size_t)st * stage_bytes;
-        const char *src = MOE ? (const char *)a.expert_out + (size_t)row * in_bytes
-                              : (const char *)a.x_in + (size_t)row * row_bytes;
-        mbar_arrive_expect_tx(&full[st], in_bytes + row_bytes);
-        bulk_g2s(dst, src, in_bytes, &full[st]);
-        bulk_g2s(dst + in_bytes, (const char *)a.h_in + (size_t)row * row_bytes, row_bytes,
-                 &full[st]);
-    };
+    const int64_t my_units = my_rows * VPT;
 
     if (tid == 0) {
-        for (int st = 0; st < stages; ++st)
+        for (int st = 0; st < stages; ++st) {
             mbar_init(&full[st], 1);
+            mbar_init(&empty[st], NC / 32);
+        }
+        fail = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0) {
-        const int64_t pre = my_rows < stages ? my_rows : stages;
-        for (int64_t i = 0; i < pre; ++i)
-            issue(i);
-    }
-    uint4 wpo[VPT], wpr[VPT];
-    load_weights<VPT>(a, wpo, wpr);
-    const bool fast_div = a.fast_div_n && weights_small<VPT>(wpo);
 
+    if (tid >= NC) {
+        // ---- producer warp: one lane issues every unit's copies ------------------------------
+        if (tid != NC)
+            return;
+        int64_t issued = 0;
+        for (int64_t u = 0; u < my_units; ++u) {
+            const int st = (int)(u % stages);
+            if (u >= stages &&
+                !mbar_wait_or_fail(&empty[st], (uint32_t)((u / stages - 1) & 1), &fail))
+                break;
+            const int64_t row = first + (u / VPT) * stride;
+            const int c = (int)(u % VPT);
+            const int nv = nvec - c * NC < NC ? nvec - c * NC : NC;
+            const uint32_t bytes = (uint32_t)nv * 16u;
+            unsigned char *dst = ring + (size_t)st * stage_bytes;
+            const size_t col = (size_t)c * kSlice;
+            mbar_arrive_expect_tx(&full[st], (uint32_t)(KIN + 1) * bytes);
+            for (int k = 0; k < KIN; ++k) {
+                const char *src = MOE ? (const char *)a.expert_out + ((size_t)row * KIN + k) * 2 * a.H
+                                      : (const char *)a.x_in + (size_t)row * 2 * a.H;
+                bulk_g2s(dst + (size_t)k * kSlice, src + col, bytes, &full[st]);
+            }
+            bulk_g2s(dst + (size_t)KIN * kSlice, (const char *)a.h_in + (size_t)row * 2 * a.H + col,
+                     bytes, &full[st]);
+            issued = u + 1;
+        }
+        // Before leaving, make sure none of this CTA's copies is still landing (bounded).
+        for (int64_t u = issued - stages > 0 ? issued - stages : 0; u < issued; ++u)
+            (void)mbar_wait(&full[u % stages], (uint32_t)((u / stages) & 1));
+        if (fail)
+            atomicOr(&g_fault_word, kFaultCopyTimeout);
+        return;
+    }
+
+    // ---- consumer warps ----------------------------------------------------------------------
+    bool fast_div = a.fast_div_n;
+    {
+        uint4 w[VPT];
+#pragma unroll
+        for (int i = 0; i < VPT; ++i)
+            w[i] = weight_vec(a.w_post, tid + i * NC, nvec);
+        fast_div = fast_div && weights_small(w);
+    }
+    const int lane = tid & 31;
     float c[kMaxK];
     for (int64_t i = 0; i < my_rows; ++i) {
-        const int st = (int)(i % stages);
-        const bool ok = mbar_wait(&full[st], (uint32_t)((i / stages) & 1));
-        if (__syncthreads_or(!ok)) {
-            // Give up: wait (bounded) for this CTA's copies still in flight, flag, return.
-            if (tid == 0) {
-                const int64_t last = i + stages < my_rows ? i + stages : my_rows;
-                for (int64_t j = i; j < last; ++j)
-                    (void)mbar_wait(&full[j % stages], (uint32_t)((j / stages) & 1));
-                atomicOr(&g_fault_word, kFaultCopyTimeout);
-            }
-            return;
-        }
-        const unsigned char *stage = ring + (size_t)st * stage_bytes;
         const int64_t row = first + i * stride;
-        if constexpr (MOE) {
-#pragma unroll
-            for (int k = 0; k < kMaxK; ++k)
-                c[k] = k < K ? __fmul_rn(a.topk_w[row * K + k], a.routed_scaling) : 0.0f;
-        }
+        if constexpr (MOE)
+            routing_coeffs(a, row, c);
         uint4 xv[VPT], hv[VPT];
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int v = tid + j * nt;
-            if (v < nvec) {
-                hv[j] = *reinterpret_cast<const uint4 *>(stage + in_bytes + 16 * v);
+        for (int ch = 0; ch < VPT; ++ch) {
+            const int64_t u = i * VPT + ch;
+            const int st = (int)(u % stages);
+            (void)mbar_wait_or_fail(&full[st], (uint32_t)((u / stages) & 1), &fail);
+            const unsigned char *stage = ring + (size_t)st * stage_bytes;
+            if (ch * NC + tid < nvec) {
+                hv[ch] = *reinterpret_cast<const uint4 *>(stage + (size_t)KIN * kSlice + 16 * tid);
                 if constexpr (MOE)
-                    xv[j] = combine_vec<true>(c, K, stage + 16 * v, row_bytes);
+                    xv[ch] = combine_vec<true>(c, KIN, stage + 16 * tid, kSlice);
                 else
-                    xv[j] = *reinterpret_cast<const uint4 *>(stage + 16 * v);
+                    xv[ch] = *reinterpret_cast<const uint4 *>(stage + 16 * tid);
             } else {
-                xv[j] = make_uint4(0u, 0u, 0u, 0u);
-                hv[j] = xv[j];
+                xv[ch] = make_uint4(0u, 0u, 0u, 0u);
+                hv[ch] = xv[ch];
             }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[st]);  // this warp is done with the stage
         }
-        // After the first block reduction every thread has read this stage: refill it.
-        boundary_chain<VPT>(a, row, xv, hv, wpo, wpr, fast_div, red, [&] {
-            if (tid == 0 && i + stages < my_rows)
-                issue(i + stages);
-        });
+        boundary_chain<VPT>(
+            a, row, xv, hv, [&](int k) { return weight_vec(a.w_post, tid + k * NC, nvec); },
+            [&](int k) { return weight_vec(a.w_pre, tid + k * NC, nvec); }, fast_div, red, NC,
+            true, [] {});
     }
+    if (tid == 0 && fail)
+        atomicOr(&g_fault_word, kFaultCopyTimeout);
 }
 
 // ---- launch ----------------------------------------------------------------------------------
@@ -354,11 +407,11 @@ int device_sms()
 }
 
 template <int VPT, bool MOE>
-cudaError_t launch_ring(const BoundaryArgs &a, int stages, uint32_t stage_bytes, int threads,
-                        int sms, cudaStream_t stream)
+cudaError_t launch_ring(const BoundaryArgs &a, int stages, size_t smem, int sms,
+                        cudaStream_t stream)
 {
-    const size_t smem = kRingHeader + (size_t)stages * stage_bytes;
     auto kern = boundary_ring_kernel<VPT, MOE>;
+    const int threads = kRingConsumers + 32;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
@@ -371,11 +424,11 @@ cudaError_t launch_ring(const BoundaryArgs &a, int stages, uint32_t stage_bytes,
         return cudaErrorInvalidConfiguration;
     const int64_t slots = (int64_t)sms * per_sm;
     const unsigned grid = (unsigned)(a.T < slots ? a.T : slots);
-    kern<<<grid, threads, smem, stream>>>(a, stages, stage_bytes);
+    kern<<<grid, threads, smem, stream>>>(a, stages);
     return cudaGetLastError();
 }
 
-// Smallest vectors-per-thread whose thread count fits both `max_threads` and the kernel's
+// Smallest vectors-per-thread whose thread count fits both `max_threads` and the rows kernel's
 // launch bound for that VPT (1024 threads at VPT 1, 512 at VPT 2 and 4, 256 at VPT 8).
 int pick_vpt(int nvec, int max_threads)
 {
@@ -391,33 +444,31 @@ int pick_vpt(int nvec, int max_threads)
 
 inline int round_warps(int n) { return (n + 31) / 32 * 32; }
 
-// Below the 227 KB per-block limit, leaving room for static shared memory.
-constexpr size_t kMaxDynSmem = 220 * 1024;
-
 template <bool MOE>
 cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
 {
     const int nvec = a.H / 8;
     const int sms = device_sms();
-    // Many rows: the persistent TMA ring, when at least two stages of inputs fit in smem.
-    if (a.T >= 4 * (int64_t)sms) {
-        const uint32_t row_bytes = 2u * (uint32_t)a.H;
-        const uint32_t stage_bytes =
-            ((MOE ? (uint32_t)a.K + 1u : 2u) * row_bytes + 127u) / 128u * 128u;
-        const int max_stages = MOE ? 2 : 4;
-        int stages = (int)((kMaxDynSmem - kRingHeader) / stage_bytes);
-        stages = stages > max_stages ? max_stages : stages;
-        if (stages >= 2) {
-            if (MOE && nvec <= 1024)
-                return launch_ring<1, MOE>(a, stages, stage_bytes, round_warps(nvec), sms, stream);
-            if (nvec <= 1024)
-                return launch_ring<2, MOE>(a, stages, stage_bytes, round_warps((nvec + 1) / 2),
-                                           sms, stream);
-            return launch_ring<4, MOE>(a, stages, stage_bytes, round_warps((nvec + 3) / 4), sms,
-                                       stream);
+    // Many rows (and rows of at most 8 chunks): the persistent warp-specialised TMA ring.
+    const int chunks = (nvec + kRingConsumers - 1) / kRingConsumers;
+    if (a.T >= 4 * (int64_t)sms && chunks <= 8) {
+        const size_t stage = (size_t)((MOE ? a.K : 1) + 1) * kRingConsumers * 16;
+        // about 54 KB of stages per CTA, so that 3-4 CTAs share an SM; at least 3, at most 16
+        int stages = (int)((54 * 1024) / stage);
+        stages = stages < 3 ? 3 : (stages > kRingMaxStages ? kRingMaxStages : stages);
+        const size_t smem = kRingHeader + stages * stage;
+        switch (chunks) {
+        case 1: return launch_ring<1, MOE>(a, stages, smem, sms, stream);
+        case 2: return launch_ring<2, MOE>(a, stages, smem, sms, stream);
+        case 3: return launch_ring<3, MOE>(a, stages, smem, sms, stream);
+        case 4: return launch_ring<4, MOE>(a, stages, smem, sms, stream);
+        case 5: return launch_ring<5, MOE>(a, stages, smem, sms, stream);
+        case 6: return launch_ring<6, MOE>(a, stages, smem, sms, stream);
+        case 7: return launch_ring<7, MOE>(a, stages, smem, sms, stream);
+        default: return launch_ring<8, MOE>(a, stages, smem, sms, stream);
         }
     }
-    // Few rows (or inputs too large to stage): one CTA per row straight from memory.
+    // Few rows (or very wide rows): one CTA per row straight from memory.
     const bool small = a.T < 2 * (int64_t)sms;
     const int max_threads = small ? 1024 : (MOE ? 320 : 256);
     const int vpt = pick_vpt(nvec, max_threads);
