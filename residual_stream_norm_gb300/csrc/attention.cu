@@ -11,11 +11,9 @@
 //  * Sigmoid output gate: [vLLM] "Attention", bullet "Sigmoid-Output-Gate"; [SGL]
 //    "混合注意力与输出门控" and the kernel-fusion paragraph (bias add, sigmoid, multiply fused).
 //
-// Q/K layout: each 16-lane half-warp owns one head of 128 elements at a time, 8 per lane (lane l
-// holds elements 8l..8l+7), so the rotation partner of element i (i + 64) sits in lane l ^ 8 of
-// the same half-warp.  A CTA of 256 threads (16 half-warps) takes tiles of TT tokens; its work
-// items are the (token, head) pairs of the tile, seven per half-warp per pass, and all loads of
-// a pass are issued before any arithmetic.  The per-token factors (64 cos/sin pairs, or the
+// Q/K layout: a CTA of 256 threads takes tiles of TT tokens; each quad of lanes owns one
+// (token, head) item of 128 elements, two items per quad per pass, all loads of a pass issued
+// before any arithmetic (see qk_norm_kernel).  The per-token factors (64 cos/sin pairs, or the
 // SSMax scale) are computed once per token into shared memory while the first loads are in
 // flight.  cos/sin are the FP32 roundings of the exact values of the FP32 angle
 // (beam_sincos.cuh), so the rotation matches the oracle bit for bit even where its two products
@@ -31,52 +29,76 @@ namespace {
 
 constexpr int kHeadDim = 128;
 constexpr int kHalf = kHeadDim / 2;
-constexpr int kIPP = 7;           // items per half-warp per pass (2 tokens x 56 heads = 112)
-constexpr int kQkThreads = 256;   // 16 half-warps
+constexpr int kQkThreads = 256;
+constexpr int kSlots = kQkThreads / 4;  // one head per quad of lanes
+constexpr int kIPP = 2;                 // heads per quad per pass, loads issued together
 
 struct RopeTable {
     float inv_freq[kHalf];  // fp32(theta^(-2i/128)), formed on the host in double
 };
 
+// Work items are the (token, head) pairs of a tile of TT tokens.  A quad of lanes owns one head:
+// lane q holds the 16-byte vectors q, q+4, q+8 and q+12 of its 128 elements, so a warp load
+// reads 64 contiguous bytes per head, and the rotation partners (element i < 64 and i + 64,
+// i.e. vectors q and q+8, q+4 and q+12) sit in the same lane.  The head's sum of squares needs a
+// two-step butterfly over the quad.  The per-token factors of the tile (64 cos/sin pairs, or
+// the SSMax scale) are computed once into shared memory while the first loads are in flight;
+// the Q and K norm weights are held in shared memory as FP32.
 template <bool ROPE, int TT>
-__global__ void __launch_bounds__(kQkThreads) qk_norm_kernel(const QkArgs a, const RopeTable tab)
+__global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, const RopeTable tab)
 {
-    // per-token factors, double-buffered by tile parity so one barrier per tile suffices
-    __shared__ __align__(16) float cs[2][TT][kHalf];
+    __shared__ __align__(16) float cs[2][TT][kHalf];  // double-buffered by tile parity
     __shared__ __align__(16) float sn[2][TT][kHalf];
     __shared__ float scale_q[2][TT];
+    __shared__ __align__(16) float wsm[2][kHeadDim];  // wq, wk as FP32
     const int nheads = a.n_q + a.n_kv;
     const int tid = threadIdx.x;
-    const int l16 = tid & 15;
-    const int hw = tid >> 4;
+    const int q = tid & 3;
+    const int slot = tid >> 2;
+    {
+        const int which = tid >> 7, e = tid & 127;
+        const bool have = which == 0 ? a.n_q > 0 : a.n_kv > 0;
+        const uint16_t *w = (const uint16_t *)(which == 0 ? a.wq : a.wk);
+        wsm[which][e] = have ? __uint_as_float((uint32_t)w[e] << 16) : 0.0f;
+    }
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    const uint4 wqv = a.n_q > 0 ? ld_cached((const char *)a.wq + 16 * l16) : zero;
-    const uint4 wkv = a.n_kv > 0 ? ld_cached((const char *)a.wk + 16 * l16) : zero;
     const int64_t ntiles = (a.T + TT - 1) / TT;
     int buf = 0;
+    __syncthreads();
 
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, buf ^= 1) {
         const int64_t t0 = tile * TT;
         const int nt = (int)(a.T - t0 < TT ? a.T - t0 : TT);
         const int nitems = nt * nheads;
 
-        for (int base = 0; base < nitems; base += 16 * kIPP) {
+        for (int base = 0; base < nitems; base += kSlots * kIPP) {
             // ---- issue the loads of this pass ------------------------------------------------
-            uint4 v[kIPP];
+            uint4 v[kIPP][4];
             char *row[kIPP];
+            int tok[kIPP], head[kIPP];
 #pragma unroll
             for (int m = 0; m < kIPP; ++m) {
-                const int j = base + hw + 16 * m;
+                const int j = base + slot + kSlots * m;
                 row[m] = nullptr;
-                v[m] = zero;
+                int tt = 0, hd = j < nitems ? j : 0;  // inactive items map to (0, 0)
+                while (hd >= nheads) {  // at most TT - 1 steps
+                    hd -= nheads;
+                    ++tt;
+                }
+                tok[m] = tt;
+                head[m] = hd;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    v[m][jj] = zero;
                 if (j < nitems) {
-                    const int tt = j / nheads, hd = j - tt * nheads;
                     const int64_t t = t0 + tt;
                     row[m] = hd < a.n_q
                                  ? (char *)a.q + 2 * (t * a.q_stride + (int64_t)hd * kHeadDim)
                                  : (char *)a.k +
                                        2 * (t * a.k_stride + (int64_t)(hd - a.n_q) * kHeadDim);
-                    v[m] = ld_plain(row[m] + 16 * l16);
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        v[m][jj] = ld_plain(row[m] + 16 * (q + 4 * jj));
                 }
             }
             // ---- per-token factors of the tile, once, while the first loads fly -------------
@@ -106,53 +128,71 @@ __global__ void __launch_bounds__(kQkThreads) qk_norm_kernel(const QkArgs a, con
             // ---- normalise, rotate / scale, round, store -----------------------------------
 #pragma unroll
             for (int m = 0; m < kIPP; ++m) {
-                const int j = base + hw + 16 * m;
-                const bool act = j < nitems;  // uniform across each half-warp
-                const int tt = act ? j / nheads : 0;
-                const int hd = act ? j - tt * nheads : 0;
-                const bool isq = hd < a.n_q;
-                const uint4 w = isq ? wqv : wkv;
-                f2 x[4];
+                const bool act = row[m] != nullptr;  // uniform across each quad
+                const int tt = tok[m];
+                const bool isq = head[m] < a.n_q;
+                f2 x[4][4];
                 Sum2x2 acc = {0ull, 0ull};
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    x[q] = widen(word(v[m], q));
-                    sum2_add(acc, mul2(x[q], x[q]));
-                }
+                for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp) {
+                        x[jj][pp] = widen(word(v[m][jj], pp));
+                        sum2_add(acc, mul2(x[jj][pp], x[jj][pp]));
+                    }
                 Sum2 tot = sum_merge(Sum2{lo_of(acc.hi), lo_of(acc.lo)},
                                      Sum2{hi_of(acc.hi), hi_of(acc.lo)});
-                tot = warp_sum(tot, 16);
+#pragma unroll
+                for (int off = 1; off < 4; off <<= 1) {
+                    Sum2 o;
+                    o.hi = __shfl_xor_sync(0xffffffffu, tot.hi, off);
+                    o.lo = __shfl_xor_sync(0xffffffffu, tot.lo, off);
+                    tot = sum_merge(tot, o);
+                }
                 const f2 rr = splat(rms_inv(sum_value(tot), (float)kHeadDim, a.eps));
-                f2 qh[4];
+                const float *wrow = wsm[isq ? 0 : 1];
+                f2 qh[4][4];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    qh[q] = mul2(mul2(x[q], rr), widen(word(w, q)));
-                f2 out[4];
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int e0 = 8 * (q + 4 * jj);
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp) {
+                        const f2 w = *reinterpret_cast<const f2 *>(&wrow[e0 + 2 * pp]);
+                        qh[jj][pp] = mul2(mul2(x[jj][pp], rr), w);
+                    }
+                }
+                f2 out[4][4];
                 if constexpr (ROPE) {
-                    const bool first_half = l16 < 8;
-                    const int fb = 8 * (l16 & 7);
-                    const f2 *c2 = reinterpret_cast<const f2 *>(&cs[buf][tt][fb]);
-                    const f2 *s2 = reinterpret_cast<const f2 *>(&sn[buf][tt][fb]);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const f2 pe = __shfl_xor_sync(0xffffffffu, qh[q], 8);
-                        const f2 qc = mul2(qh[q], c2[q]);
-                        const f2 ps = mul2(pe, s2[q]);
-                        // first half: q_i c - q_{i+64} s;  second half: q_{i+64} c + q_i s
-                        out[q] = first_half ? sub2(qc, ps) : add2(qc, ps);
+                    for (int jj = 0; jj < 2; ++jj) {
+                        const int i0 = 8 * (q + 4 * jj);  // first-half element index (< 64)
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp) {
+                            const f2 c = *reinterpret_cast<const f2 *>(&cs[buf][tt][i0 + 2 * pp]);
+                            const f2 sv = *reinterpret_cast<const f2 *>(&sn[buf][tt][i0 + 2 * pp]);
+                            const f2 lo = qh[jj][pp], hi = qh[jj + 2][pp];
+                            // out_i = q_i c - q_{i+64} s;  out_{i+64} = q_{i+64} c + q_i s
+                            out[jj][pp] = sub2(mul2(lo, c), mul2(hi, sv));
+                            out[jj + 2][pp] = add2(mul2(hi, c), mul2(lo, sv));
+                        }
                     }
                 } else {
-                    const f2 sc = isq ? splat(scale_q[buf][tt]) : splat(1.0f);
+                    const f2 sc = splat(isq ? scale_q[buf][tt] : 1.0f);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        out[q] = isq ? mul2(qh[q], sc) : qh[q];
+                    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp)
+                            out[jj][pp] = isq ? mul2(qh[jj][pp], sc) : qh[jj][pp];
                 }
                 if (act) {
-                    uint4 o;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        word(o, q) = narrow(out[q]);
-                    st_global(row[m] + 16 * l16, o);
+                    for (int jj = 0; jj < 4; ++jj) {
+                        uint4 o;
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp)
+                            word(o, pp) = narrow(out[jj][pp]);
+                        st_global(row[m] + 16 * (q + 4 * jj), o);
+                    }
                 }
             }
         }

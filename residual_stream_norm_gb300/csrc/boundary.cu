@@ -296,6 +296,8 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
     const int tid = threadIdx.x;
     const int KIN = MOE ? a.K : 1;
     const uint32_t stage_bytes = (uint32_t)(KIN + 1) * kSlice;
+    // each consumer thread parks its slices of w_post and w_pre here: [2][VPT][NC] vectors
+    uint4 *wsm = reinterpret_cast<uint4 *>(ring + (size_t)stages * stage_bytes);
     const int64_t first = blockIdx.x;
     const int64_t stride = gridDim.x;
     const int64_t my_rows = first < a.T ? (a.T - first + stride - 1) / stride : 0;
@@ -350,16 +352,29 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
     {
         uint4 w[VPT];
 #pragma unroll
-        for (int i = 0; i < VPT; ++i)
+        for (int i = 0; i < VPT; ++i) {
             w[i] = weight_vec(a.w_post, tid + i * NC, nvec);
+            wsm[i * NC + tid] = w[i];
+            wsm[(VPT + i) * NC + tid] = weight_vec(a.w_pre, tid + i * NC, nvec);
+        }
         fast_div = fast_div && weights_small(w);
     }
     const int lane = tid & 31;
-    float c[kMaxK];
+    float c[kMaxK], c_next[kMaxK];
+    if constexpr (MOE) {
+        if (my_rows > 0)
+            routing_coeffs(a, first, c_next);
+    }
     for (int64_t i = 0; i < my_rows; ++i) {
         const int64_t row = first + i * stride;
-        if constexpr (MOE)
-            routing_coeffs(a, row, c);
+        if constexpr (MOE) {
+            // this row's coefficients were fetched during the previous row; fetch the next's
+#pragma unroll
+            for (int k = 0; k < kMaxK; ++k)
+                c[k] = c_next[k];
+            if (i + 1 < my_rows)
+                routing_coeffs(a, row + stride, c_next);
+        }
         uint4 xv[VPT], hv[VPT];
 #pragma unroll
         for (int ch = 0; ch < VPT; ++ch) {
@@ -382,9 +397,8 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
                 mbar_arrive(&empty[st]);  // this warp is done with the stage
         }
         boundary_chain<VPT>(
-            a, row, xv, hv, [&](int k) { return weight_vec(a.w_post, tid + k * NC, nvec); },
-            [&](int k) { return weight_vec(a.w_pre, tid + k * NC, nvec); }, fast_div, red, NC,
-            true, [] {});
+            a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
+            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, fast_div, red, NC, true, [] {});
     }
     if (tid == 0 && fail)
         atomicOr(&g_fault_word, kFaultCopyTimeout);
@@ -453,10 +467,12 @@ cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
     const int chunks = (nvec + kRingConsumers - 1) / kRingConsumers;
     if (a.T >= 4 * (int64_t)sms && chunks <= 8) {
         const size_t stage = (size_t)((MOE ? a.K : 1) + 1) * kRingConsumers * 16;
-        // about 54 KB of stages per CTA, so that 3-4 CTAs share an SM; at least 3, at most 16
-        int stages = (int)((54 * 1024) / stage);
+        const size_t weights = (size_t)2 * chunks * kRingConsumers * 16;
+        // stages: about 32 KB per CTA for the plain boundary (4 CTAs per SM), 3 for the MoE
+        // variant (whose stages hold K + 1 slices); at most 16
+        int stages = MOE ? 3 : (int)((32 * 1024) / stage);
         stages = stages < 3 ? 3 : (stages > kRingMaxStages ? kRingMaxStages : stages);
-        const size_t smem = kRingHeader + stages * stage;
+        const size_t smem = kRingHeader + stages * stage + weights;
         switch (chunks) {
         case 1: return launch_ring<1, MOE>(a, stages, smem, sms, stream);
         case 2: return launch_ring<2, MOE>(a, stages, smem, sms, stream);
