@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
             so.orc_bf16_rne_array.argtypes = [f32p, u16p, i64]
             so.orc_residual_scales.argtypes = [i32, f32p, f32p]
             so.orc_rope_inv_freq.argtypes = [f32, i32, f32p]
+            so.orc_exact_sum_f32.argtypes = [f32p, i64]
+            so.orc_exact_sum_f32.restype = f32
             so.orc_ssmax_scale.argtypes = [i64, f32, f32]
             so.orc_ssmax_scale.restype = f32
             so.orc_boundary.argtypes = [u16p, u16p, u16p, u16p, u16p, u16p, i64, i32, i32, f32,
@@ -110,6 +112,12 @@ def bf16_to_f32(b) -> np.ndarray:
     """BF16 bit patterns -> FP32 values (exact widening)."""
     b = np.ascontiguousarray(b, dtype=np.uint16)
     return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def exact_sum_f32(terms) -> float:
+    """The FP32 rounding (nearest even) of the exact sum of non-negative FP32 terms."""
+    t = _f32(terms)
+    return lib().orc_exact_sum_f32(_ptr(t, ctypes.c_float), t.size)
 
 
 def residual_scales(n: int) -> tuple[float, float]:

@@ -6,9 +6,9 @@
  * CUDA library (no headers, helpers or tables); the two meet only on the seeded inputs.
  *
  * Every function works one token at a time, in program order, in FP32 arithmetic with the BF16
- * round-to-nearest-even points the pages state.  Two steps are deliberately more accurate than a
- * GPU can afford, so the oracle is the exact side of every comparison:
- *   - a row's sum of squares is accumulated in double and rounded once to FP32;
+ * round-to-nearest-even points the pages state.  Two steps are computed as their exact values
+ * rounded once, so the oracle is the exact side of every comparison:
+ *   - a row's sum of squares is summed exactly (integer fixed point) and rounded once to FP32;
  *   - exp / cos / sin / pow are evaluated in double and rounded once to FP32.
  * Build with -ffp-contract=off: a contracted multiply-add would change the FP32 rounding steps.
  *
@@ -63,22 +63,116 @@ void orc_bf16_rne_array(const float *in, uint16_t *out, int64_t count)
 /* RMSNorm scale                                                                               */
 /* ------------------------------------------------------------------------------------------ */
 
+/* Exact sum of non-negative FP32 terms, rounded once to FP32 with round-to-nearest-even.
+ * Every finite FP32 value is an integer multiple of 2^-149 (the smallest subnormal), so the
+ * terms are added exactly as integers in a 384-bit fixed-point accumulator (a Kulisch
+ * accumulator: bit i of the integer is worth 2^(i-149)); the result is rounded once.  A NaN term
+ * makes the sum NaN, an infinite term (and no NaN) makes it +inf. */
+typedef struct {
+    uint64_t limb[6];
+    int nan, inf;
+} exact_sum;
+
+static void exact_sum_init(exact_sum *a)
+{
+    memset(a, 0, sizeof *a);
+}
+
+static void exact_sum_add(exact_sum *a, float t)
+{
+    uint32_t u;
+    memcpy(&u, &t, sizeof u);
+    uint32_t e = (u >> 23) & 0xffu;
+    uint64_t m = u & 0x7fffffu;
+    if (e == 0xffu) {
+        if (m)
+            a->nan = 1;
+        else
+            a->inf = 1;
+        return;
+    }
+    if (e)
+        m |= 0x800000u;      /* normal: t = m * 2^(e - 150) = m * 2^(e - 1) * 2^-149 */
+    else
+        e = 1;               /* subnormal: t = m * 2^-149 */
+    uint32_t p = e - 1;      /* bit position of m's lowest bit */
+    uint32_t li = p / 64, sh = p % 64;
+    unsigned __int128 v = (unsigned __int128)m << sh;
+    uint64_t lo = (uint64_t)v, hi = (uint64_t)(v >> 64);
+    uint64_t before = a->limb[li];
+    a->limb[li] += lo;
+    uint64_t carry = a->limb[li] < before;
+    for (uint32_t k = li + 1; k < 6 && (hi || carry); ++k) {
+        before = a->limb[k];
+        a->limb[k] += hi + carry;
+        carry = (a->limb[k] < before) || (carry && hi + carry == 0);
+        hi = 0;
+    }
+}
+
+static int exact_sum_bit(const exact_sum *a, int i)
+{
+    return i < 0 ? 0 : (int)((a->limb[i / 64] >> (i % 64)) & 1u);
+}
+
+static float exact_sum_round(const exact_sum *a)
+{
+    if (a->nan)
+        return NAN;
+    if (a->inf)
+        return INFINITY;
+    int top = -1;
+    for (int i = 6 * 64 - 1; i >= 0; --i)
+        if (exact_sum_bit(a, i)) {
+            top = i;
+            break;
+        }
+    if (top < 0)
+        return 0.0f;
+    if (top < 24)  /* fewer than 25 significant bits: exactly representable */
+        return ldexpf((float)a->limb[0], -149);
+    uint32_t mant = 0;
+    for (int i = top; i > top - 24; --i)
+        mant = (mant << 1) | (uint32_t)exact_sum_bit(a, i);
+    int half = exact_sum_bit(a, top - 24), sticky = 0;
+    for (int i = top - 25; i >= 0 && !sticky; --i)
+        sticky = exact_sum_bit(a, i);
+    if (half && (sticky || (mant & 1u))) {
+        mant += 1;
+        if (mant == (1u << 24)) {
+            mant >>= 1;
+            top += 1;
+        }
+    }
+    return ldexpf((float)mant, (top - 23) - 149);  /* exact, or +inf past the FP32 range */
+}
+
 /* r = 1 / sqrt(mean_j v_j^2 + eps).
- * Each square is an FP32 product; the squares are summed in double (for BF16 inputs every term
- * is exact and the double sum is exact to ~1e-13 relative) and the sum is rounded once to FP32;
- * the mean is that FP32 sum divided by the length in FP32; then FP32 add, IEEE sqrt, IEEE div.
+ * Each square is an FP32 product; their exact sum is rounded once to FP32; the mean is that FP32
+ * sum divided by the length in FP32; then FP32 add, IEEE sqrt, IEEE div.
  * [vLLM] "MoE und Residual-Stream", bullet "Sandwich-Norm": an RMSNorm before and after every
  * sublayer; [vLLM] "Agentengetriebene Optimierung", change 1: FP32 math. */
 static float rms_inv(const float *v, int32_t len, float eps)
 {
-    double acc = 0.0;
+    exact_sum acc;
+    exact_sum_init(&acc);
     for (int32_t j = 0; j < len; ++j) {
         float sq = v[j] * v[j];
-        acc += (double)sq;
+        exact_sum_add(&acc, sq);
     }
-    float ms = (float)acc;
+    float ms = exact_sum_round(&acc);
     float mean = ms / (float)len;
     return 1.0f / sqrtf(mean + eps);
+}
+
+/* Test hook: the exactly rounded FP32 sum of `count` non-negative FP32 terms. */
+float orc_exact_sum_f32(const float *terms, int64_t count)
+{
+    exact_sum acc;
+    exact_sum_init(&acc);
+    for (int64_t i = 0; i < count; ++i)
+        exact_sum_add(&acc, terms[i]);
+    return exact_sum_round(&acc);
 }
 
 /* ------------------------------------------------------------------------------------------ */

@@ -213,3 +213,59 @@ def test_combine_then_boundary_is_the_boundary_chain():
                                                 c["w_pre"], n=10, return_x=True)
     h2, y2, r2 = oracle.boundary(c["h"], x, c["w_post"], c["w_pre"], n=10)
     assert np.array_equal(h1, h2) and np.array_equal(y1, y2) and np.array_equal(r1, r2)
+
+
+# ------------------------------------------------------------------------------------------
+# the exact row sum (the sum of squares is taken exactly and rounded once to FP32)
+# ------------------------------------------------------------------------------------------
+
+def _nearest_f32(fr):
+    """FP32 nearest to a non-negative Fraction, ties to even (exact selection by comparison)."""
+    from fractions import Fraction
+    c = np.float32(float(fr))
+    cands = {c, np.nextafter(c, np.float32(np.inf)), np.nextafter(c, np.float32(0))}
+    best = None
+    for v in sorted(cands):
+        d = abs(Fraction(float(v)) - fr)
+        key = (d, int(np.array(v, np.float32).view(np.uint32)) & 1)
+        if best is None or key < best[0]:
+            best = (key, v)
+    return best[1]
+
+
+def test_exact_sum_matches_rational_arithmetic():
+    from fractions import Fraction
+    g = np.random.Generator(np.random.PCG64(3))
+    cases = [
+        [1.0, 2.0 ** -24],                       # exact tie: stays on the even neighbour
+        [1.0, 2.0 ** -24, 2.0 ** -60],           # just above the tie: up (double sum misses it)
+        [1.0, 2.0 ** -24, 2.0 ** -149],          # above the tie by one subnormal
+        [1.0 + 2.0 ** -23, 2.0 ** -24],          # tie, odd neighbour: up
+        [2.0 ** -149] * 7,                       # subnormal sum
+        [3.0e38, 3.0e38],                        # overflow to inf
+        [],
+        list(g.standard_normal(5120).astype(np.float32) ** 2),
+        list((g.standard_normal(4096) * 2.0 ** g.integers(-60, 60, 4096)).astype(np.float32) ** 2),
+    ]
+    for terms in cases:
+        t = np.array(terms, dtype=np.float32)
+        got = oracle.exact_sum_f32(t)
+        exact = sum((Fraction(float(v)) for v in t), Fraction(0))
+        want = np.float32(np.inf) if exact > Fraction(float(np.finfo(np.float32).max)) * \
+            (1 + Fraction(1, 2 ** 25)) else _nearest_f32(exact)
+        assert np.float32(got) == want, (terms[:4], got, want)
+    assert np.isnan(oracle.exact_sum_f32(np.array([1.0, np.nan], np.float32)))
+    assert oracle.exact_sum_f32(np.array([1.0, np.inf], np.float32)) == np.inf
+
+
+def test_near_tie_row_sum_rounds_up():
+    # squares 1, 2^-24, 2^-60 of BF16 values 1, 2^-12, 2^-30: the exact sum lies just above the
+    # midpoint between 1 and 1 + 2^-23, so its FP32 rounding is 1 + 2^-23.
+    H = 8
+    x = np.zeros((1, H), np.float32)
+    x[0, :3] = [1.0, 2.0 ** -12, 2.0 ** -30]
+    xb = oracle.bf16_rne(x)
+    ones = oracle.bf16_rne(np.ones(H, np.float32))
+    _, _, rstd = oracle.boundary(np.zeros_like(xb), xb, ones, ones, n=1, eps=0.0)
+    ms = np.float32(1.0 + 2.0 ** -23)
+    assert rstd[0, 0] == np.float32(1.0) / np.sqrt(ms / np.float32(H))
