@@ -149,7 +149,25 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
                     o.lo = __shfl_xor_sync(0xffffffffu, tot.lo, off);
                     tot = sum_merge(tot, o);
                 }
-                const f2 rr = splat(rms_inv(sum_value(tot), (float)kHeadDim, a.eps));
+                float ms = sum_value(tot);
+                const bool tie = near_tie(tot.hi, tot.lo, ms);
+                if (__any_sync(0xffffffffu, tie)) {
+                    // rare: recompute this head's sum exactly (double-double) so that its FP32
+                    // rounding is that of the exact sum; the whole warp joins the shuffles
+                    DD d = {0.0, 0.0};
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp) {
+                            const float lo = lo_of(x[jj][pp]), hi = hi_of(x[jj][pp]);
+                            d = dd_add(d, (double)__fmul_rn(lo, lo));
+                            d = dd_add(d, (double)__fmul_rn(hi, hi));
+                        }
+                    d = dd_warp_sum(d, 4);
+                    if (tie)
+                        ms = dd_to_float(d);
+                }
+                const f2 rr = splat(rms_inv(ms, (float)kHeadDim, a.eps));
                 const float *wrow = wsm[isq ? 0 : 1];
                 f2 qh[4][4];
 #pragma unroll

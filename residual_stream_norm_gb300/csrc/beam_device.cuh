@@ -109,13 +109,16 @@ __device__ __forceinline__ void sum_add(Sum2 &acc, float t)
 }
 
 // Commutative merge: merge(a, b) and merge(b, a) give identical bits, so butterfly shuffles
-// leave every lane with the same value.
+// leave every lane with the same value.  The result is renormalised (|lo| <= ulp(hi) / 2), so
+// each merge adds at most ~2 u^2 |sum| of error however many terms it carries (u = 2^-24).
 __device__ __forceinline__ Sum2 sum_merge(Sum2 a, Sum2 b)
 {
+    float s, e;
+    two_sum(a.hi, b.hi, s, e);
+    const float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), e);
     Sum2 r;
-    float e;
-    two_sum(a.hi, b.hi, r.hi, e);
-    r.lo = __fadd_rn(__fadd_rn(a.lo, b.lo), e);
+    r.hi = __fadd_rn(s, lo);  // Dekker's fast two-sum: |s| >= |lo|
+    r.lo = __fsub_rn(lo, __fsub_rn(r.hi, s));
     return r;
 }
 
@@ -140,19 +143,79 @@ __device__ __forceinline__ Sum2 warp_sum(Sum2 a, int width = 32)
     return a;
 }
 
-// Block-wide sum; `slot` is a shared array of >= blockDim.x/32 entries that no other
-// reduction of the same phase uses.  Every thread returns the same value.
-__device__ __forceinline__ float block_sum(Sum2 a, Sum2 *slot)
+// ---------------------------------------------------------------------------------------------
+// Exact rounding of a row sum.
+//
+// The compensated sums above are within 2^-37 relative of the exact sum of their (non-negative,
+// exactly computed) terms: at most n^2/2 u^2 from a thread's n-term accumulation (n <= 64 here)
+// plus ~2 u^2 per merge level.  RN(hi + lo) is then the FP32 rounding of the exact sum unless
+// hi + lo lies within that distance of a rounding boundary; near_tie() detects those rows
+// (about 2^-12 of them) so that they can be recomputed in double-double, whose error (~2^-100)
+// cannot change the rounding.
+// ---------------------------------------------------------------------------------------------
+
+// True when RN(hi + lo) = r1 might not be the rounding of the exact sum.
+__device__ __forceinline__ bool near_tie(float hi, float lo, float r1)
 {
-    a = warp_sum(a);
-    const int nw = blockDim.x >> 5;
-    if ((threadIdx.x & 31) == 0)
-        slot[threadIdx.x >> 5] = a;
-    __syncthreads();
-    Sum2 r = slot[0];
-    for (int w = 1; w < nw; ++w)
-        r = sum_merge(r, slot[w]);
-    return sum_value(r);
+    if (!(r1 > 0.0f) || !isfinite(r1))
+        return false;  // zero (all terms zero) or non-finite: nothing to decide
+    const uint32_t u = __float_as_uint(r1);
+    const uint32_t e = u >> 23;
+    if (e < 40u)
+        return true;  // tiny sums always take the exact path
+    const float half_up = __uint_as_float((e - 24u) << 23);  // ulp(r1) / 2
+    const float half_dn = (u & 0x7fffffu) ? half_up : __uint_as_float((e - 25u) << 23);
+    const float band = __uint_as_float((e - 36u) << 23);     // >= 2^-37 r1
+    const float res = __fadd_rn(__fsub_rn(hi, r1), lo);     // hi - r1 is exact
+    return res > __fsub_rn(half_up, band) || res < __fsub_rn(band, half_dn);
+}
+
+// Double-double accumulator (Knuth's TwoSum in FP64) for the rare exact path.
+struct DD {
+    double hi, lo;
+};
+
+__device__ __forceinline__ DD dd_add(DD a, double t)
+{
+    const double s = __dadd_rn(a.hi, t);
+    const double bp = __dsub_rn(s, a.hi);
+    const double e = __dadd_rn(__dsub_rn(a.hi, __dsub_rn(s, bp)), __dsub_rn(t, bp));
+    return DD{s, __dadd_rn(a.lo, e)};
+}
+
+__device__ __forceinline__ DD dd_merge(DD a, DD b)
+{
+    DD r = dd_add(a, b.hi);
+    r.lo = __dadd_rn(r.lo, b.lo);
+    const double h = __dadd_rn(r.hi, r.lo);
+    return DD{h, __dsub_rn(r.lo, __dsub_rn(h, r.hi))};
+}
+
+__device__ __forceinline__ DD dd_warp_sum(DD a, int width = 32)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        if (off < width) {
+            DD o;
+            o.hi = __shfl_xor_sync(0xffffffffu, a.hi, off);
+            o.lo = __shfl_xor_sync(0xffffffffu, a.lo, off);
+            a = dd_merge(a, o);
+        }
+    }
+    return a;
+}
+
+// FP32 rounding (nearest even) of hi + lo for a renormalised pair: |lo| <= ulp(hi)/2, so lo can
+// only decide when hi is exactly a midpoint between two FP32 values.
+__device__ __forceinline__ float dd_to_float(DD a)
+{
+    float f = __double2float_rn(a.hi);
+    if (a.lo != 0.0) {
+        const float fd = __double2float_rd(a.hi), fu = __double2float_ru(a.hi);
+        if (fd != fu && a.hi == 0.5 * ((double)fd + (double)fu))
+            f = a.lo > 0.0 ? fu : fd;
+    }
+    return f;
 }
 
 // r = 1 / sqrt(ms / len + eps) with IEEE division and square root.

@@ -41,11 +41,15 @@ namespace {
 
 constexpr int kMaxK = 16;
 
-// Block-wide sum over `nt` threads (a multiple of 32).  `named`: synchronise only those
-// threads on named barrier 1 (the ring kernel's consumer warps); otherwise __syncthreads.
-// Warp partials go through `slot` (>= 32 entries no concurrent reduction uses); every warp
-// combines them with the same butterfly, so all threads get identical bits.
-__device__ __forceinline__ float block_sum_w(Sum2 a, Sum2 *slot, int nt, bool named)
+// Block-wide sum over `nt` threads (a multiple of 32), rounded as the exact sum would be.
+// `named`: synchronise only those threads on named barrier 1 (the ring kernel's consumer
+// warps); otherwise __syncthreads.  Warp partials go through `slot` / `dslot` (>= 32 entries no
+// concurrent reduction uses); every warp combines them with the same butterfly, so all threads
+// get identical bits and take the rare exact path (exact_partial(): this thread's terms summed
+// in double-double) together.
+template <typename ExactPartial>
+__device__ __forceinline__ float block_sum_w(Sum2 a, Sum2 *slot, DD *dslot, int nt, bool named,
+                                             ExactPartial exact_partial)
 {
     a = warp_sum(a);
     const int lane = threadIdx.x & 31;
@@ -68,7 +72,38 @@ __device__ __forceinline__ float block_sum_w(Sum2 a, Sum2 *slot, int nt, bool na
     }
     p.hi = __shfl_sync(0xffffffffu, p.hi, 0);
     p.lo = __shfl_sync(0xffffffffu, p.lo, 0);
-    return sum_value(p);
+    const float r1 = sum_value(p);
+    if (!near_tie(p.hi, p.lo, r1))
+        return r1;
+    // rare: the row sum is within the compensated sum's error of an FP32 rounding boundary
+    DD d = dd_warp_sum(exact_partial());
+    if (lane == 0)
+        dslot[threadIdx.x >> 5] = d;
+    if (named)
+        named_sync(1, nt);
+    else
+        __syncthreads();
+    DD q = lane < nw ? dslot[lane] : DD{0.0, 0.0};
+    q = dd_warp_sum(q);
+    q.hi = __shfl_sync(0xffffffffu, q.hi, 0);
+    q.lo = __shfl_sync(0xffffffffu, q.lo, 0);
+    return dd_to_float(q);
+}
+
+// This thread's squares of packed BF16 vectors, summed in double-double (the exact path).
+template <int VPT>
+__device__ __forceinline__ DD squares_dd(const uint4 (&v)[VPT])
+{
+    DD d = {0.0, 0.0};
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const f2 x = widen(word(v[i], j));
+            d = dd_add(d, (double)__fmul_rn(lo_of(x), lo_of(x)));
+            d = dd_add(d, (double)__fmul_rn(hi_of(x), hi_of(x)));
+        }
+    return d;
 }
 
 __device__ __forceinline__ Sum2 lanes_merged(const Sum2x2 &a)
@@ -99,8 +134,8 @@ template <int VPT, typename WPost, typename WPre, typename AfterFirstSum>
 __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t row,
                                                const uint4 (&xv)[VPT], const uint4 (&hv)[VPT],
                                                WPost wpo, WPre wpr, bool fast_div,
-                                               Sum2 (*red)[32], int nt, bool named,
-                                               AfterFirstSum after_first_sum)
+                                               Sum2 (*red)[32], DD (*dred)[32], int nt,
+                                               bool named, AfterFirstSum after_first_sum)
 {
     const int nvec = a.H >> 3;
     const int tid = threadIdx.x;
@@ -116,7 +151,9 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
             sum2_add(acc, mul2(x, x));
         }
     }
-    const float r = rms_inv(block_sum_w(lanes_merged(acc), red[0], nt, named), (float)a.H, a.eps);
+    const float r = rms_inv(
+        block_sum_w(lanes_merged(acc), red[0], dred[0], nt, named, [&] { return squares_dd(xv); }),
+        (float)a.H, a.eps);
     after_first_sum();
 
     // ---- a1 / a2: xhat = bf16((x r) w_post); h' = bf16(bf16(alpha h) + bf16(xhat / s)) -----
@@ -157,8 +194,9 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
             }
         }
     }
-    const f2 rr2 =
-        splat(rms_inv(block_sum_w(lanes_merged(acc), red[1], nt, named), (float)a.H, a.eps));
+    const f2 rr2 = splat(rms_inv(
+        block_sum_w(lanes_merged(acc), red[1], dred[1], nt, named, [&] { return squares_dd(hp); }),
+        (float)a.H, a.eps));
 
     // ---- a3: y = bf16((h' r') w_pre); store h' and y -----------------------------------------
     char *h_out = (char *)a.h_out + 2 * row_off;
@@ -225,6 +263,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
     boundary_rows_kernel(const BoundaryArgs a)
 {
     __shared__ Sum2 red[2][32];
+    __shared__ DD dred[2][32];
     const int nvec = a.H >> 3;
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
@@ -261,7 +300,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
         }
         boundary_chain<VPT>(
             a, row, xv, hv, [&](int i) { return wpo[i]; }, [&](int i) { return wpr[i]; },
-            fast_div, red, nt, false, [] {});
+            fast_div, red, dred, nt, false, [] {});
     }
 }
 
@@ -288,6 +327,7 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
     uint64_t *empty = full + kRingMaxStages;
     unsigned char *ring = dyn + kRingHeader;
     __shared__ Sum2 red[2][32];
+    __shared__ DD dred[2][32];
     __shared__ int fail;
 
     constexpr int NC = kRingConsumers;
@@ -398,7 +438,8 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
         }
         boundary_chain<VPT>(
             a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
-            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, fast_div, red, NC, true, [] {});
+            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, fast_div, red, dred, NC, true,
+            [] {});
     }
     if (tid == 0 && fail)
         atomicOr(&g_fault_word, kFaultCopyTimeout);

@@ -171,3 +171,23 @@ def test_zero_tokens():
     a = torch.empty((0, 48 * D), dtype=torch.bfloat16, device="cuda")
     rsn.beam_attn_gate_fwd(a, a, a, torch.zeros(48, device="cuda"), 48, D)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("kind", ["rope", "ssmax"])
+@pytest.mark.parametrize("T", [3, 400])
+def test_near_tie_head_sums_round_exactly(kind, T):
+    # heads whose sum of squares sits at or just above an FP32 rounding boundary
+    c = bi.attn_qk_case(T=T, seed=41)
+    g = np.random.Generator(np.random.PCG64(7))
+    q = np.zeros((T, bi.N_Q_HEADS, D), np.float32)
+    k = np.zeros((T, bi.N_KV_HEADS, D), np.float32)
+    tiny = [0.0, 2.0 ** -30, 2.0 ** -40, 2.0 ** -60]
+    for arr in (q, k):
+        for idx in np.ndindex(arr.shape[:2]):
+            cols = g.choice(D, size=3, replace=False)
+            arr[idx][cols] = [1.0, 2.0 ** -12, tiny[(idx[0] + idx[1]) % 4]]
+    c["q"] = bi.from_u16(oracle.bf16_rne(q))
+    c["k"] = bi.from_u16(oracle.bf16_rne(k))
+    qo, ko = run_qk(kind, c)
+    wq, wk = oracle_qk(kind, c)
+    assert np.array_equal(u16(qo), wq) and np.array_equal(u16(ko), wk)

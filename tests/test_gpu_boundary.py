@@ -209,3 +209,28 @@ def test_no_device_faults_raised():
     # The persistent kernels bound every wait on their own copies; none may have given up.
     torch.cuda.synchronize()
     assert rsn.beam_device_faults() == 0
+
+
+def _near_tie_rows(T, H, seed):
+    """Rows whose sum of squares lies at or within 2^-60 relative of an FP32 rounding boundary
+    (squares 1, 2^-24 and a tiny third term), so that only an exactly rounded sum gets r right."""
+    g = np.random.Generator(np.random.PCG64(seed))
+    x = np.zeros((T, H), np.float32)
+    tiny = [0.0, 2.0 ** -30, 2.0 ** -40, 2.0 ** -60]
+    for t in range(T):
+        cols = g.choice(H, size=3, replace=False)
+        base = [1.0, 1.0 + 2.0 ** -7][t % 2]          # even or odd FP32 neighbour below
+        x[t, cols] = [base, 2.0 ** -12, tiny[t % 4] * (1 if g.random() < 0.5 else -1)]
+    return oracle.bf16_rne(x)
+
+
+@pytest.mark.parametrize("T", [7, 700])
+def test_near_tie_row_sums_round_exactly(T):
+    H = 5120
+    xb = _near_tie_rows(T, H, seed=T)
+    c = bi.boundary_case(T=T, n=3, seed=14)
+    h = u16(c["h"])
+    got = run_gpu(bi.from_u16(h), bi.from_u16(xb), c["w_post"], c["w_pre"], 3)
+    want = oracle.boundary(h, xb, u16(c["w_post"]), u16(c["w_pre"]), 3)
+    assert np.array_equal(got[2][:, 0], want[2][:, 0]), "r must be the exactly rounded value"
+    check(got, want, f"near-tie rows T={T}")
