@@ -189,9 +189,16 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
                             const f2 c = *reinterpret_cast<const f2 *>(&cs[buf][tt][i0 + 2 * pp]);
                             const f2 sv = *reinterpret_cast<const f2 *>(&sn[buf][tt][i0 + 2 * pp]);
                             const f2 lo = qh[jj][pp], hi = qh[jj + 2][pp];
-                            // out_i = q_i c - q_{i+64} s;  out_{i+64} = q_{i+64} c + q_i s
-                            out[jj][pp] = sub2(mul2(lo, c), mul2(hi, sv));
-                            out[jj + 2][pp] = add2(mul2(hi, c), mul2(lo, sv));
+                            // out_i = q_i c - q_{i+64} s;  out_{i+64} = q_{i+64} c + q_i s.
+                            // Scalar IEEE intrinsics: a packed product feeding a packed add is
+                            // fused into one FMA by the compiler, which would skip the rounding
+                            // of the products.
+                            out[jj][pp] = make_f2(
+                                __fsub_rn(__fmul_rn(lo_of(lo), lo_of(c)), __fmul_rn(lo_of(hi), lo_of(sv))),
+                                __fsub_rn(__fmul_rn(hi_of(lo), hi_of(c)), __fmul_rn(hi_of(hi), hi_of(sv))));
+                            out[jj + 2][pp] = make_f2(
+                                __fadd_rn(__fmul_rn(lo_of(hi), lo_of(c)), __fmul_rn(lo_of(lo), lo_of(sv))),
+                                __fadd_rn(__fmul_rn(hi_of(hi), hi_of(c)), __fmul_rn(hi_of(lo), hi_of(sv))));
                         }
                     }
                 } else {

@@ -115,6 +115,8 @@ __device__ __forceinline__ Sum2 sum_merge(Sum2 a, Sum2 b)
 {
     float s, e;
     two_sum(a.hi, b.hi, s, e);
+    if (!isfinite(s))  // overflow or a non-finite term: the IEEE sum is s itself
+        return Sum2{s, 0.0f};
     const float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), e);
     Sum2 r;
     r.hi = __fadd_rn(s, lo);  // Dekker's fast two-sum: |s| >= |lo|

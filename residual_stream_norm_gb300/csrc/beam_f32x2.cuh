@@ -4,6 +4,12 @@
 // Each .f32x2 instruction applies the IEEE round-to-nearest FP32 operation to both lanes, so a
 // packed computation gives bit-for-bit the results of the scalar one at half the instruction
 // count.  A pair holds BF16 elements 2i (low lane) and 2i+1 (high lane) of one 32-bit word.
+//
+// Caution: the compiler fuses a packed product that feeds a packed add/sub into one packed FMA
+// (the product is then not rounded), despite the .rn modifiers and even through an opaque move.
+// Packed products therefore only feed packed adds where the product is exact (squares of BF16
+// values); an inexact product followed by an add uses the scalar __fmul_rn / __fadd_rn
+// intrinsics, which are never fused.
 #pragma once
 
 #include <cmath>
