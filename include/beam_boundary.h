@@ -24,6 +24,12 @@
  *  - Arithmetic is FP32 with IEEE division and square root; results are rounded to BF16 with
  *    round-to-nearest-even exactly at the points each call lists.
  *  - Aliasing: only the overlaps each call names are allowed; any other overlap is undefined.
+ *  - Launch order: kernels are launched with programmatic dependent launch.  A kernel may start
+ *    while the preceding kernel on the same stream is still running, and it reads its model
+ *    parameters (norm weights w_post / w_pre / wq / wk, the gate bias) before waiting for that
+ *    kernel; every other input is read, and every output written, only after the preceding
+ *    kernel has completed.  So the norm weights and the gate bias must not be written by the
+ *    kernel launched immediately before on the same stream.
  */
 #ifndef BEAM_BOUNDARY_H
 #define BEAM_BOUNDARY_H

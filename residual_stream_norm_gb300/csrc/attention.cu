@@ -55,7 +55,8 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
     const int tid = threadIdx.x;
     const int q = tid & 3;
     const int slot = tid >> 2;
-    {
+    pdl_launch_dependents();
+    {  // model parameters: fetched before waiting on the previous kernel
         const int which = tid >> 7, e = tid & 127;
         const bool have = which == 0 ? a.n_q > 0 : a.n_kv > 0;
         const uint16_t *w = (const uint16_t *)(which == 0 ? a.wq : a.wk);
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
     const int64_t ntiles = (a.T + TT - 1) / TT;
     int buf = 0;
     __syncthreads();
+    pdl_wait();
 
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, buf ^= 1) {
         const int64_t t0 = tile * TT;
@@ -234,6 +236,8 @@ __global__ void __launch_bounds__(256) attn_gate_kernel(const GateArgs a)
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
     const f2 one = splat(1.0f);
+    pdl_launch_dependents();
+    pdl_wait();
     for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
         const char *attn = (const char *)a.attn + 2 * t * a.attn_stride;
         const char *gate = (const char *)a.gate + 2 * t * a.gate_stride;
@@ -281,11 +285,13 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
     for (int i = 0; i < kHalf; ++i)
         tab.inv_freq[i] = ROPE ? a.inv_freq_host[i] : 0.0f;
     // Few tokens: one token per CTA spreads them over more SMs; otherwise two per CTA.
-    if (a.T < 2 * 152)
-        qk_norm_kernel<ROPE, 1><<<grid_for(a.T), kQkThreads, 0, stream>>>(a, tab);
-    else
-        qk_norm_kernel<ROPE, 2><<<grid_for((a.T + 1) / 2), kQkThreads, 0, stream>>>(a, tab);
-    return cudaGetLastError();
+    const cudaError_t e =
+        a.T < 2 * 152
+            ? launch_pdl(qk_norm_kernel<ROPE, 1>, dim3(grid_for(a.T)), dim3(kQkThreads), 0, stream,
+                         a, tab)
+            : launch_pdl(qk_norm_kernel<ROPE, 2>, dim3(grid_for((a.T + 1) / 2)), dim3(kQkThreads),
+                         0, stream, a, tab);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
@@ -306,8 +312,9 @@ cudaError_t launch_attn_gate(const GateArgs &a, cudaStream_t stream)
     int threads = (vpr + 3) / 4;
     threads = threads > 256 ? 256 : threads;
     threads = (threads + 31) / 32 * 32;
-    attn_gate_kernel<<<grid_for(a.T), threads, 0, stream>>>(a);
-    return cudaGetLastError();
+    const cudaError_t e =
+        launch_pdl(attn_gate_kernel, dim3(grid_for(a.T)), dim3(threads), 0, stream, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace beam

@@ -220,6 +220,23 @@ __device__ __forceinline__ float dd_to_float(DD a)
     return f;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel lets the next kernel of its stream be scheduled
+// as soon as it starts (launch_dependents), and reads nothing but model parameters (norm
+// weights, gate bias) before griddepcontrol.wait, which returns once the preceding kernel has
+// completed and its writes are visible.  Without a programmatic launch both are no-ops.
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // r = 1 / sqrt(ms / len + eps) with IEEE division and square root.
 __device__ __forceinline__ float rms_inv(float ms, float len, float eps)
 {

@@ -267,13 +267,15 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
     const int nvec = a.H >> 3;
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
-    uint4 wpo[VPT], wpr[VPT];
+    pdl_launch_dependents();
+    uint4 wpo[VPT], wpr[VPT];  // model parameters: fetched before waiting on the previous kernel
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         wpo[i] = weight_vec(a.w_post, tid + i * nt, nvec);
         wpr[i] = weight_vec(a.w_pre, tid + i * nt, nvec);
     }
     const bool fast_div = a.fast_div_n && weights_small(wpo);
+    pdl_wait();
 
     for (int64_t row = blockIdx.x; row < a.T; row += gridDim.x) {
         const int64_t row_off = row * (int64_t)a.H;
@@ -336,13 +338,15 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
     const int tid = threadIdx.x;
     const int KIN = MOE ? a.K : 1;
     const uint32_t stage_bytes = (uint32_t)(KIN + 1) * kSlice;
-    // each consumer thread parks its slices of w_post and w_pre here: [2][VPT][NC] vectors
+    // the plain boundary's consumer threads park their slices of w_post and w_pre here
+    // ([2][VPT][NC] vectors); the MoE variant, whose stages are large, reads them through L1
     uint4 *wsm = reinterpret_cast<uint4 *>(ring + (size_t)stages * stage_bytes);
     const int64_t first = blockIdx.x;
     const int64_t stride = gridDim.x;
     const int64_t my_rows = first < a.T ? (a.T - first + stride - 1) / stride : 0;
     const int64_t my_units = my_rows * VPT;
 
+    pdl_launch_dependents();
     if (tid == 0) {
         for (int st = 0; st < stages; ++st) {
             mbar_init(&full[st], 1);
@@ -357,6 +361,7 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
         // ---- producer warp: one lane issues every unit's copies ------------------------------
         if (tid != NC)
             return;
+        pdl_wait();
         int64_t issued = 0;
         for (int64_t u = 0; u < my_units; ++u) {
             const int st = (int)(u % stages);
@@ -394,11 +399,14 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             w[i] = weight_vec(a.w_post, tid + i * NC, nvec);
-            wsm[i * NC + tid] = w[i];
-            wsm[(VPT + i) * NC + tid] = weight_vec(a.w_pre, tid + i * NC, nvec);
+            if constexpr (!MOE) {
+                wsm[i * NC + tid] = w[i];
+                wsm[(VPT + i) * NC + tid] = weight_vec(a.w_pre, tid + i * NC, nvec);
+            }
         }
         fast_div = fast_div && weights_small(w);
     }
+    pdl_wait();
     const int lane = tid & 31;
     float c[kMaxK], c_next[kMaxK];
     if constexpr (MOE) {
@@ -436,10 +444,16 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
             if (lane == 0)
                 mbar_arrive(&empty[st]);  // this warp is done with the stage
         }
-        boundary_chain<VPT>(
-            a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
-            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, fast_div, red, dred, NC, true,
-            [] {});
+        if constexpr (MOE)
+            boundary_chain<VPT>(
+                a, row, xv, hv, [&](int k) { return weight_vec(a.w_post, tid + k * NC, nvec); },
+                [&](int k) { return weight_vec(a.w_pre, tid + k * NC, nvec); }, fast_div, red,
+                dred, NC, true, [] {});
+        else
+            boundary_chain<VPT>(
+                a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
+                [&](int k) { return wsm[(VPT + k) * NC + tid]; }, fast_div, red, dred, NC, true,
+                [] {});
     }
     if (tid == 0 && fail)
         atomicOr(&g_fault_word, kFaultCopyTimeout);
@@ -479,8 +493,8 @@ cudaError_t launch_ring(const BoundaryArgs &a, int stages, size_t smem, int sms,
         return cudaErrorInvalidConfiguration;
     const int64_t slots = (int64_t)sms * per_sm;
     const unsigned grid = (unsigned)(a.T < slots ? a.T : slots);
-    kern<<<grid, threads, smem, stream>>>(a, stages);
-    return cudaGetLastError();
+    e = launch_pdl(kern, dim3(grid), dim3(threads), smem, stream, a, stages);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Smallest vectors-per-thread whose thread count fits both `max_threads` and the rows kernel's
@@ -508,7 +522,7 @@ cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
     const int chunks = (nvec + kRingConsumers - 1) / kRingConsumers;
     if (a.T >= 4 * (int64_t)sms && chunks <= 8) {
         const size_t stage = (size_t)((MOE ? a.K : 1) + 1) * kRingConsumers * 16;
-        const size_t weights = (size_t)2 * chunks * kRingConsumers * 16;
+        const size_t weights = MOE ? 0 : (size_t)2 * chunks * kRingConsumers * 16;
         // stages: about 32 KB per CTA for the plain boundary (4 CTAs per SM), 3 for the MoE
         // variant (whose stages hold K + 1 slices); at most 16
         int stages = MOE ? 3 : (int)((32 * 1024) / stage);
@@ -531,13 +545,14 @@ cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
     const int vpt = pick_vpt(nvec, max_threads);
     const int threads = round_warps((nvec + vpt - 1) / vpt);
     const dim3 grid((unsigned)(a.T < (int64_t)(1 << 30) ? a.T : (int64_t)(1 << 30)));
+    cudaError_t e;
     switch (vpt) {
-    case 1: boundary_rows_kernel<1, MOE><<<grid, threads, 0, stream>>>(a); break;
-    case 2: boundary_rows_kernel<2, MOE><<<grid, threads, 0, stream>>>(a); break;
-    case 4: boundary_rows_kernel<4, MOE><<<grid, threads, 0, stream>>>(a); break;
-    default: boundary_rows_kernel<8, MOE><<<grid, threads, 0, stream>>>(a); break;
+    case 1: e = launch_pdl(boundary_rows_kernel<1, MOE>, grid, dim3(threads), 0, stream, a); break;
+    case 2: e = launch_pdl(boundary_rows_kernel<2, MOE>, grid, dim3(threads), 0, stream, a); break;
+    case 4: e = launch_pdl(boundary_rows_kernel<4, MOE>, grid, dim3(threads), 0, stream, a); break;
+    default: e = launch_pdl(boundary_rows_kernel<8, MOE>, grid, dim3(threads), 0, stream, a); break;
     }
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace
