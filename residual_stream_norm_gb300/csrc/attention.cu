@@ -44,6 +44,23 @@ struct RopeTable {
 // two-step butterfly over the quad.  The per-token factors of the tile (64 cos/sin pairs, or
 // the SSMax scale) are computed once into shared memory while the first loads are in flight;
 // the Q and K norm weights are held in shared memory as FP32.
+// The rare exact path: this quad's head sum of squares in double-double, rounded once to FP32
+// (every lane of the warp calls it; the shuffles stay within quads).
+__device__ __forceinline__ float head_sum_exact(const uint4 (&v)[4])
+{
+    DD d = {0.0, 0.0};
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+            const uint32_t w = word(v[jj], pp);
+            const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+            d = dd_add(d, (double)__fmul_rn(lo, lo));
+            d = dd_add(d, (double)__fmul_rn(hi, hi));
+        }
+    return dd_to_float(dd_warp_sum(d, 4));
+}
+
 template <bool ROPE, int TT>
 __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, const RopeTable tab)
 {
@@ -156,18 +173,9 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
                 if (__any_sync(0xffffffffu, tie)) {
                     // rare: recompute this head's sum exactly (double-double) so that its FP32
                     // rounding is that of the exact sum; the whole warp joins the shuffles
-                    DD d = {0.0, 0.0};
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                        for (int pp = 0; pp < 4; ++pp) {
-                            const float lo = lo_of(x[jj][pp]), hi = hi_of(x[jj][pp]);
-                            d = dd_add(d, (double)__fmul_rn(lo, lo));
-                            d = dd_add(d, (double)__fmul_rn(hi, hi));
-                        }
-                    d = dd_warp_sum(d, 4);
+                    const float exact = head_sum_exact(v[m]);
                     if (tie)
-                        ms = dd_to_float(d);
+                        ms = exact;
                 }
                 const f2 rr = splat(rms_inv(ms, (float)kHeadDim, a.eps));
                 const float *wrow = wsm[isq ? 0 : 1];

@@ -130,6 +130,18 @@ __device__ __forceinline__ uint32_t narrow(f2 v)
     return d;
 }
 
+// bf16(float(a) + float(b)) for two BF16 pairs, as one packed BF16 add.  For two BF16 operands
+// the FP32 sum is exact unless their exponents differ by 16 or more, and then the smaller one is
+// far below half a BF16 ulp of the larger, so rounding the FP32 sum to BF16 and rounding the
+// exact sum to BF16 give the same value: the correctly rounded BF16 sum that add.rn.bf16x2
+// returns.
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Packed compensated sum: two independent Knuth TwoSum accumulators, one per lane.
 struct Sum2x2 {
     f2 hi, lo;

@@ -41,6 +41,26 @@ namespace {
 
 constexpr int kMaxK = 16;
 
+// The rare exact path of block_sum_w: the block's double-double sum, rounded once to FP32.
+// Kept out of line so that the hot loops stay small in the instruction cache.
+__device__ __noinline__ float block_sum_exact(DD d, DD *dslot, int nt, bool named)
+{
+    const int lane = threadIdx.x & 31;
+    const int nw = nt >> 5;
+    d = dd_warp_sum(d);
+    if (lane == 0)
+        dslot[threadIdx.x >> 5] = d;
+    if (named)
+        named_sync(1, nt);
+    else
+        __syncthreads();
+    DD q = lane < nw ? dslot[lane] : DD{0.0, 0.0};
+    q = dd_warp_sum(q);
+    q.hi = __shfl_sync(0xffffffffu, q.hi, 0);
+    q.lo = __shfl_sync(0xffffffffu, q.lo, 0);
+    return dd_to_float(q);
+}
+
 // Block-wide sum over `nt` threads (a multiple of 32), rounded as the exact sum would be.
 // `named`: synchronise only those threads on named barrier 1 (the ring kernel's consumer
 // warps); otherwise __syncthreads.  Warp partials go through `slot` / `dslot` (>= 32 entries no
@@ -76,18 +96,7 @@ __device__ __forceinline__ float block_sum_w(Sum2 a, Sum2 *slot, DD *dslot, int 
     if (!near_tie(p.hi, p.lo, r1))
         return r1;
     // rare: the row sum is within the compensated sum's error of an FP32 rounding boundary
-    DD d = dd_warp_sum(exact_partial());
-    if (lane == 0)
-        dslot[threadIdx.x >> 5] = d;
-    if (named)
-        named_sync(1, nt);
-    else
-        __syncthreads();
-    DD q = lane < nw ? dslot[lane] : DD{0.0, 0.0};
-    q = dd_warp_sum(q);
-    q.hi = __shfl_sync(0xffffffffu, q.hi, 0);
-    q.lo = __shfl_sync(0xffffffffu, q.lo, 0);
-    return dd_to_float(q);
+    return block_sum_exact(exact_partial(), dslot, nt, named);
 }
 
 // This thread's squares of packed BF16 vectors, summed in double-double (the exact path).
@@ -187,7 +196,7 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t aw = narrow(mul2(al, widen(word(hv[i], j))));
-                const uint32_t hq = narrow(add2(widen(aw), widen(bw[j])));
+                const uint32_t hq = add_bf16x2(aw, bw[j]);  // bf16(a + b)
                 word(hp[i], j) = hq;
                 const f2 hf = widen(hq);
                 sum2_add(acc, mul2(hf, hf));
@@ -221,19 +230,32 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
 // x = bf16(sum_k c_k e_k) for one 16-byte vector: one FMA per slot in slot order from +0.
 // `e0` points at slot 0 of this vector; slots are `slot_bytes` apart.
 template <bool SMEM>
+__device__ __forceinline__ void combine_slot(f2 (&acc)[4], float ck, const unsigned char *p)
+{
+    const uint4 ev = SMEM ? *reinterpret_cast<const uint4 *>(p) : ld_stream(p);
+    const f2 c2 = splat(ck);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        acc[j] = fma2(c2, widen(word(ev, j)), acc[j]);
+}
+
+template <bool SMEM>
 __device__ __forceinline__ uint4 combine_vec(const float (&c)[kMaxK], int K,
                                              const unsigned char *e0, size_t slot_bytes)
 {
     f2 acc[4] = {0ull, 0ull, 0ull, 0ull};
+    if (K == 8) {  // Beam's top-8: fully unrolled
 #pragma unroll
-    for (int k = 0; k < kMaxK; ++k) {
-        if (k < K) {
-            const unsigned char *p = e0 + (size_t)k * slot_bytes;
-            const uint4 ev = SMEM ? *reinterpret_cast<const uint4 *>(p) : ld_stream(p);
-            const f2 ck = splat(c[k]);
+        for (int k = 0; k < 8; ++k)
+            combine_slot<SMEM>(acc, c[k], e0 + (size_t)k * slot_bytes);
+    } else {
+#pragma unroll 1
+        for (int k = 0; k < K; ++k) {
+            float ck = c[0];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                acc[j] = fma2(ck, widen(word(ev, j)), acc[j]);
+            for (int kk = 1; kk < kMaxK; ++kk)  // register-resident select of c[k]
+                ck = kk == k ? c[kk] : ck;
+            combine_slot<SMEM>(acc, ck, e0 + (size_t)k * slot_bytes);
         }
     }
     uint4 x;
