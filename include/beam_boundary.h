@@ -77,13 +77,15 @@ BEAM_API int beam_residual_scales(int32_t n, float *alpha, float *s);
  * No counterpart on the pages: a diagnostic of this library. */
 BEAM_API int beam_device_faults(uint32_t *flags, int clear);
 
-/* Host-only helper: the FP32 quotient x / s (s = fp32(sqrt(n))) exactly as the boundary kernels
- * form it before rounding b = bf16(x / s): for n <= 4096 and 2^-99 <= |x| < inf by Markstein's
- * FMA correction step (y = RN(1/s), q = RN(x y), q' = RN(q + (x - q s) y)), otherwise by IEEE
- * division; the result equals IEEE division for every finite BF16 x (checked exhaustively by the
- * tests).  `count` values in host memory.  Returns BEAM_ERR_INVALID_ARG for n < 1, count < 0 or
- * NULL arrays. */
-BEAM_API int beam_residual_quotient(const float *x, float *q_out, int64_t count, int32_t n);
+/* Host-only helper: the residual operand b = bf16(x / s), s = fp32(sqrt(n)), returned as FP32
+ * values, for `count` BF16 values x given as FP32 (low 16 bits zero) in host memory, exactly as
+ * the boundary kernels form it ("Tiefenskalierte Residuen").  The kernels take b = bf16(RN(x y))
+ * with y = RN(1/s) when that is known to equal bf16(RN(x / s)) -- for this n, checked over all
+ * 128 BF16 significands, and x above an exponent floor so that both values are normal -- and IEEE
+ * division otherwise; the result equals bf16 of the IEEE quotient for every BF16 x (checked
+ * exhaustively by the tests).  Returns BEAM_ERR_INVALID_ARG for n < 1, count < 0 or NULL
+ * arrays, and for inputs that are not BF16 values (their outputs are NaN). */
+BEAM_API int beam_residual_operand(const float *x, float *b_out, int64_t count, int32_t n);
 
 /* Host-only helper: the FP32 cosine and sine that beam_qk_norm_rope_fwd uses for an FP32 rotary
  * angle, for `count` angles in host memory.  Each value is the FP32 rounding of the exact

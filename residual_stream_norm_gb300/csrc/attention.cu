@@ -234,13 +234,20 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
     }
 }
 
+// Head of vector v: floor(v / vph), vph = head_dim / 8 vectors per head, as floor(v * m / 2^32)
+// with m = ceil(2^32 / vph) (gate_head_magic()).  With e = m * vph - 2^32 < vph the quotient is
+// exact whenever v * e < 2^32; here v < 1024 * vph and vph <= 128, so v * e < 2^24.
+__device__ __forceinline__ int gate_head(int v, uint64_t m)
+{
+    return (int)(((uint64_t)(uint32_t)v * m) >> 32);
+}
+
 // out = bf16(attn * 1/(1 + expf(-(gate + bias_h)))).  One CTA per row, 4 vectors per thread
 // per pass, all loads of a pass issued before any arithmetic; the additions, the reciprocal's
 // operand and the product run on packed pairs, expf and the IEEE reciprocal per element.
 __global__ void __launch_bounds__(256) attn_gate_kernel(const GateArgs a)
 {
     const int vpr = (a.n_heads * a.head_dim) >> 3;
-    const int vph = a.head_dim >> 3;
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
     const f2 one = splat(1.0f);
@@ -264,7 +271,7 @@ __global__ void __launch_bounds__(256) attn_gate_kernel(const GateArgs a)
             for (int i = 0; i < 4; ++i) {
                 const int v = v0 + tid + i * nt;
                 if (v < vpr) {
-                    const f2 b = splat(a.bias[v / vph]);
+                    const f2 b = splat(a.bias[gate_head(v, a.head_magic)]);
                     uint4 o;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -312,6 +319,12 @@ cudaError_t launch_qk_norm_rope(const QkArgs &a, cudaStream_t stream)
 cudaError_t launch_qk_norm_ssmax(const QkArgs &a, cudaStream_t stream)
 {
     return launch_qk<false>(a, stream);
+}
+
+uint64_t gate_head_magic(int32_t head_dim)
+{
+    const uint64_t vph = (uint64_t)(head_dim / 8);
+    return ((1ull << 32) + vph - 1) / vph;
 }
 
 cudaError_t launch_attn_gate(const GateArgs &a, cudaStream_t stream)

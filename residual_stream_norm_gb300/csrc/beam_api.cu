@@ -41,6 +41,22 @@ const float *rope_inv_freq(float theta)
     return table;
 }
 
+// The residual operand rule of the boundary kernels for this n (beam_f32x2.cuh).  The check of
+// the 128 significands is cached per thread for the last residual index.
+void set_residual_rule(beam::BoundaryArgs &a)
+{
+    static thread_local float cached_s = -1.0f;
+    static thread_local bool cached_ok = false;
+    a.inv_s = 1.0f / a.s;
+    if (a.s != cached_s) {
+        cached_ok = beam::residual_mul_exact(a.s, a.inv_s);
+        cached_s = a.s;
+    }
+    a.mul_div = cached_ok;
+    const uint32_t f = beam::residual_floor_exp(a.s);
+    a.floor_bits = (f << 7) | (f << 23);
+}
+
 int check_qk(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride, const void *wq,
              const void *wk, const int64_t *pos, int64_t T, int32_t n_q, int32_t n_kv,
              int32_t head_dim, float eps)
@@ -100,16 +116,26 @@ int beam_device_faults(uint32_t *flags, int clear)
     return cuda_status(e);
 }
 
-int beam_residual_quotient(const float *x, float *q_out, int64_t count, int32_t n)
+int beam_residual_operand(const float *x, float *b_out, int64_t count, int32_t n)
 {
-    if (n < 1 || count < 0 || (count > 0 && (!x || !q_out)))
+    if (n < 1 || count < 0 || (count > 0 && (!x || !b_out)))
         return BEAM_ERR_INVALID_ARG;
-    float alpha, s;
-    beam_residual_scales(n, &alpha, &s);
-    const float y = 1.0f / s;
-    for (int64_t i = 0; i < count; ++i)
-        q_out[i] = beam::residual_quotient_host(x[i], n, s, y);
-    return BEAM_OK;
+    beam::BoundaryArgs a{};
+    beam_residual_scales(n, &a.alpha, &a.s);
+    set_residual_rule(a);
+    const uint32_t f = a.floor_bits >> 23;
+    int st = BEAM_OK;
+    for (int64_t i = 0; i < count; ++i) {
+        uint32_t u;
+        std::memcpy(&u, &x[i], sizeof u);
+        if (u & 0xffffu) {  // not a BF16 value
+            b_out[i] = NAN;
+            st = BEAM_ERR_INVALID_ARG;
+            continue;
+        }
+        b_out[i] = beam::residual_operand_host(x[i], a.s, a.inv_s, a.mul_div, f);
+    }
+    return st;
 }
 
 int beam_rope_cos_sin(const float *angle, float *cos_out, float *sin_out, int64_t count)
@@ -155,8 +181,7 @@ int beam_boundary_fwd(void *h_out, void *y_out, const void *h_in, const void *x_
     a.K = 0;
     a.eps = eps;
     beam_residual_scales(n, &a.alpha, &a.s);
-    a.inv_s = 1.0f / a.s;
-    a.fast_div_n = n <= beam::kMarksteinMaxN;
+    set_residual_rule(a);
     return cuda_status(beam::launch_boundary(a, stream));
 }
 
@@ -192,8 +217,7 @@ int beam_moe_combine_boundary_fwd(void *h_out, void *y_out, const void *h_in,
     a.K = K;
     a.eps = eps;
     beam_residual_scales(n, &a.alpha, &a.s);
-    a.inv_s = 1.0f / a.s;
-    a.fast_div_n = n <= beam::kMarksteinMaxN;
+    set_residual_rule(a);
     return cuda_status(beam::launch_moe_boundary(a, stream));
 }
 
@@ -284,6 +308,7 @@ int beam_attn_gate_fwd(void *out, const void *attn, const void *gate, const floa
     a.attn_stride = attn_row_stride;
     a.gate_stride = gate_row_stride;
     a.out_stride = out_row_stride;
+    a.head_magic = beam::gate_head_magic(head_dim);
     return cuda_status(beam::launch_attn_gate(a, stream));
 }
 

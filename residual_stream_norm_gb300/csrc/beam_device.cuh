@@ -100,28 +100,18 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
     e = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bp));
 }
 
-__device__ __forceinline__ void sum_add(Sum2 &acc, float t)
-{
-    float s, e;
-    two_sum(acc.hi, t, s, e);
-    acc.hi = s;
-    acc.lo = __fadd_rn(acc.lo, e);
-}
-
-// Commutative merge: merge(a, b) and merge(b, a) give identical bits, so butterfly shuffles
-// leave every lane with the same value.  The result is renormalised (|lo| <= ulp(hi) / 2), so
-// each merge adds at most ~2 u^2 |sum| of error however many terms it carries (u = 2^-24).
+// Commutative merge: merge(a, b) and merge(b, a) give identical bits (TwoSum's error term is
+// the unique exact remainder), so butterfly shuffles leave every lane with the same value.  The
+// pair is not renormalised: lo gathers the exact TwoSum errors and the incoming lo terms, so after
+// L merges |lo| stays within about L/2 ulp(hi), and each of its additions errs by at most
+// 2^-24 |lo| -- far below the 2^-37 budget of near_tie() -- while the dependent chain per merge
+// stays short.  A non-finite hi propagates as in IEEE addition (lo then becomes NaN and is
+// ignored by sum_value()).
 __device__ __forceinline__ Sum2 sum_merge(Sum2 a, Sum2 b)
 {
     float s, e;
     two_sum(a.hi, b.hi, s, e);
-    if (!isfinite(s))  // overflow or a non-finite term: the IEEE sum is s itself
-        return Sum2{s, 0.0f};
-    const float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), e);
-    Sum2 r;
-    r.hi = __fadd_rn(s, lo);  // Dekker's fast two-sum: |s| >= |lo|
-    r.lo = __fsub_rn(lo, __fsub_rn(r.hi, s));
-    return r;
+    return Sum2{s, __fadd_rn(__fadd_rn(a.lo, b.lo), e)};
 }
 
 // FP32 value of the sum.  Once hi has overflowed (or a term was inf / NaN) the error term is
@@ -149,8 +139,9 @@ __device__ __forceinline__ Sum2 warp_sum(Sum2 a, int width = 32)
 // Exact rounding of a row sum.
 //
 // The compensated sums above are within 2^-37 relative of the exact sum of their (non-negative,
-// exactly computed) terms: at most n^2/2 u^2 from a thread's n-term accumulation (n <= 64 here)
-// plus ~2 u^2 per merge level.  RN(hi + lo) is then the FP32 rounding of the exact sum unless
+// exactly computed) terms: an accumulator of m terms errs by at most m^2/2 u^2 (u = 2^-24; a
+// thread splits its n <= 64 terms over two accumulators, n^2/4 u^2 <= 2^-38) and each of at most
+// ten merge levels by about 5 u^2 more.  RN(hi + lo) is the FP32 rounding of the exact sum unless
 // hi + lo lies within that distance of a rounding boundary; near_tie() detects those rows
 // (about 2^-12 of them) so that they can be recomputed in double-double, whose error (~2^-100)
 // cannot change the rounding.

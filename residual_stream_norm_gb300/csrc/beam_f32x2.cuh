@@ -1,5 +1,5 @@
 // beam_f32x2.cuh -- packed FP32 pair arithmetic (sm_100+ add/mul/fma .f32x2) for the
-// boundary-path kernels, and the residual operand division shared with the host.
+// boundary-path kernels, and the residual operand rule shared with the host.
 //
 // Each .f32x2 instruction applies the IEEE round-to-nearest FP32 operation to both lanes, so a
 // packed computation gives bit-for-bit the results of the scalar one at half the instruction
@@ -19,53 +19,61 @@
 namespace beam {
 
 // ---------------------------------------------------------------------------------------------
-// x / s for the depth-scaled residual operand b = bf16(x / s), s = fp32(sqrt(n)).
+// The depth-scaled residual operand b = bf16(x / s), s = fp32(sqrt(n)), for a BF16 value x.
 //
-// Markstein's correction step (P. Markstein, IBM J. Res. Dev. 34(1), 1990; also Cornea,
-// Harrison and Tang, "Scientific Computing on Itanium-based Systems", 2002): with y = RN(1/s),
-// q = RN(x * y), the remainder rem = x - q * s is exact when formed by one FMA (barring
-// underflow), and q' = RN(q + rem * y) is the correctly rounded quotient.  The kernels use it for
-// BF16 x with |x| >= 2^-99 (exponent field >= kMarksteinMinExp) and residual index
-// n <= kMarksteinMaxN -- checked exhaustively against IEEE division for every such x and n; the
-// step loses the sign of -0 and, for |x| below ~2^-109, the remainder is no longer exact, so
-// smaller (and zero) x use IEEE division.  An infinite x would give NaN (inf - inf); the
-// kernels take the fast path only when every |w_post| < 2^120, so that
-// x = bf16((x_in * r) * w_post) cannot overflow (|x_in * r| <= sqrt(H)).  NaN stays NaN.
+// With y = RN(1/s), the single product RN(x y) is not always the IEEE quotient RN(x / s), but
+// after the rounding to BF16 the two agree for every BF16 significand at most residual indices
+// (n = 810 and 3240 are the only exceptions up to 4096).  Whether they do for a given n is a
+// finite check over the 128 BF16 significands of [1, 2) (residual_mul_exact), and it carries over
+// to every x = M 2^E whose product and quotient are normal FP32 numbers, because scaling by a
+// power of two commutes with both roundings there.  That is the case when the biased exponent of
+// x is at least residual_floor_exp(s); zero, subnormal and tiny x fall below it.  The kernels
+// multiply where both conditions hold and divide (IEEE) elsewhere.  inf * y = inf / s, and NaN
+// stays NaN either way.
 // ---------------------------------------------------------------------------------------------
 
-constexpr int32_t kMarksteinMaxN = 4096;
-constexpr uint32_t kMarksteinMinExp = 28;   // biased exponent of 2^-99
-constexpr uint32_t kWeightMaxExp = 247;     // biased exponent of 2^120
-
-#if defined(__CUDACC__)
-#define BEAM_F2_HD __host__ __device__ __forceinline__
-#else
-#define BEAM_F2_HD inline
-#endif
-
-BEAM_F2_HD float div_markstein(float x, float s, float y)
+// BF16 bits of v, round to nearest even (NaN stays NaN) -- host side.
+inline uint32_t bf16_bits_host(float v)
 {
-#if defined(__CUDA_ARCH__)
-    const float q = __fmul_rn(x, y);
-    const float rem = __fmaf_rn(q, -s, x);
-    return __fmaf_rn(rem, y, q);
-#else
-    const float q = x * y;
-    const float rem = std::fma(q, -s, x);
-    return std::fma(rem, y, q);
-#endif
+    uint32_t u;
+    std::memcpy(&u, &v, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u)
+        return (u >> 16) | 0x40u;
+    return (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
 }
 
-// The kernels' rule for one BF16 value x (given as FP32): the correction step where it is
-// exact, IEEE division elsewhere (host reference of the device code path).
-inline float residual_quotient_host(float x, int32_t n, float s, float y)
+// True when bf16(RN(m y)) == bf16(RN(m / s)) for every BF16 significand m in [1, 2) (and, as a
+// margin, in [2, 4)).
+inline bool residual_mul_exact(float s, float y)
+{
+    for (int k = 128; k < 512; ++k) {
+        const float m = (float)k / 128.0f;  // exact
+        if (bf16_bits_host(m * y) != bf16_bits_host(m / s))
+            return false;
+    }
+    return true;
+}
+
+// Smallest biased FP32 exponent e such that every |x| >= 2^(e - 127) has a normal product x y
+// and quotient x / s: e = 1 + c with 2^c >= 2 s.
+inline uint32_t residual_floor_exp(float s)
+{
+    uint32_t c = 0;
+    while (std::ldexp(1.0f, (int)c) < 2.0f * s)
+        ++c;
+    return 1u + c;
+}
+
+// The kernels' rule for one BF16 value x (given as FP32), as a host reference: b as FP32.
+inline float residual_operand_host(float x, float s, float y, bool mul_ok, uint32_t floor_exp)
 {
     uint32_t u;
     std::memcpy(&u, &x, sizeof u);
     const uint32_t e = (u >> 23) & 0xffu;
-    if (n <= kMarksteinMaxN && e >= kMarksteinMinExp && e < 0xffu)
-        return div_markstein(x, s, y);
-    return x / s;
+    const uint32_t b = bf16_bits_host(mul_ok && e >= floor_exp ? x * y : x / s) << 16;
+    float r;
+    std::memcpy(&r, &b, sizeof r);
+    return r;
 }
 
 #if defined(__CUDACC__)
@@ -157,21 +165,23 @@ __device__ __forceinline__ void sum2_add(Sum2x2 &a, f2 t)
     a.lo = add2(a.lo, e);
 }
 
-// x / s on a pair by the correction step above (y = RN(1/s), neg_s = -s, both splatted).
-__device__ __forceinline__ f2 div2_markstein(f2 x, f2 neg_s, f2 y)
+// Merge of two packed accumulators (TwoSum of the hi parts, error added to the lo parts).
+__device__ __forceinline__ Sum2x2 sum2_merge(const Sum2x2 &a, const Sum2x2 &b)
 {
-    const f2 q = mul2(x, y);
-    const f2 rem = fma2(q, neg_s, x);
-    return fma2(rem, y, q);
+    const f2 s = add2(a.hi, b.hi);
+    const f2 bp = sub2(s, a.hi);
+    const f2 ap = sub2(s, bp);
+    const f2 e = add2(sub2(a.hi, ap), sub2(b.hi, bp));
+    return Sum2x2{s, add2(add2(a.lo, b.lo), e)};
 }
 
-// Accumulates into `all` a word whose bits 15 and 31 stay set only if both BF16 lanes of `w`
-// have an exponent field >= kMarksteinMinExp (a borrow trick on each 16-bit half; the halves
-// cannot borrow from each other because each starts at 0x8000 or more).
-__device__ __forceinline__ void exp_floor_check(uint32_t &all, uint32_t w)
+// Bit 15 of each 16-bit half stays set only if that BF16 element of `w` has an exponent field
+// >= f, where floor_bits = (f << 7) | (f << 23) (a borrow trick on each half; the halves cannot
+// borrow from each other because each starts at 0x8000 or more).  AND the results of several
+// words and test them with exp_floor_ok().
+__device__ __forceinline__ uint32_t exp_floor_bits(uint32_t w, uint32_t floor_bits)
 {
-    constexpr uint32_t kFloor = (kMarksteinMinExp << 7) | (kMarksteinMinExp << 23);
-    all &= ((w & 0x7f807f80u) | 0x80008000u) - kFloor;
+    return ((w & 0x7f807f80u) | 0x80008000u) - floor_bits;
 }
 
 __device__ __forceinline__ bool exp_floor_ok(uint32_t all)

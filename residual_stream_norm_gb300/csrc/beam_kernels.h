@@ -41,8 +41,9 @@ struct BoundaryArgs {
     float routed_scaling;
     float alpha;             // fp32(sqrt((n-1)/n))
     float s;                 // fp32(sqrt(n))
-    float inv_s;             // fp32(1 / s), IEEE division on the host
-    bool fast_div_n;         // n small enough for the Markstein division step
+    float inv_s;             // y = fp32(1 / s), IEEE division on the host
+    bool mul_div;            // residual_mul_exact(s, y): b = bf16(x y) where x is above the floor
+    uint32_t floor_bits;     // (f << 7) | (f << 23), f = residual_floor_exp(s)
     float eps;
 };
 
@@ -76,6 +77,7 @@ struct GateArgs {
     int64_t attn_stride;
     int64_t gate_stride;
     int64_t out_stride;
+    uint64_t head_magic;  // gate_head_magic(head_dim)
 };
 
 cudaError_t launch_boundary(const BoundaryArgs &a, cudaStream_t stream);
@@ -83,6 +85,8 @@ cudaError_t launch_moe_boundary(const BoundaryArgs &a, cudaStream_t stream);
 cudaError_t launch_qk_norm_rope(const QkArgs &a, cudaStream_t stream);
 cudaError_t launch_qk_norm_ssmax(const QkArgs &a, cudaStream_t stream);
 cudaError_t launch_attn_gate(const GateArgs &a, cudaStream_t stream);
+// ceil(2^32 / (head_dim / 8)): the multiplier that maps a gate vector index to its head.
+uint64_t gate_head_magic(int32_t head_dim);
 
 // The device fault word of the current device (bit 0: a kernel gave up waiting for its own bulk
 // copies); synchronous.

@@ -41,12 +41,23 @@ namespace {
 
 constexpr int kMaxK = 16;
 
-// The rare exact path of block_sum_w: the block's double-double sum, rounded once to FP32.
-// Kept out of line so that the hot loops stay small in the instruction cache.
-__device__ __noinline__ float block_sum_exact(DD d, DD *dslot, int nt, bool named)
+// The rare exact path of block_sum_sq: the block's sum of squares of the threads' vectors in
+// double-double, rounded once to FP32.
+template <int VPT>
+__device__ __forceinline__ float block_sum_exact(const uint4 (&v)[VPT], DD *dslot, int nt,
+                                                 bool named)
 {
     const int lane = threadIdx.x & 31;
     const int nw = nt >> 5;
+    DD d = {0.0, 0.0};
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const f2 x = widen(word(v[i], j));
+            d = dd_add(d, (double)__fmul_rn(lo_of(x), lo_of(x)));
+            d = dd_add(d, (double)__fmul_rn(hi_of(x), hi_of(x)));
+        }
     d = dd_warp_sum(d);
     if (lane == 0)
         dslot[threadIdx.x >> 5] = d;
@@ -61,17 +72,22 @@ __device__ __noinline__ float block_sum_exact(DD d, DD *dslot, int nt, bool name
     return dd_to_float(q);
 }
 
-// Block-wide sum over `nt` threads (a multiple of 32), rounded as the exact sum would be.
-// `named`: synchronise only those threads on named barrier 1 (the ring kernel's consumer
+__device__ __forceinline__ Sum2 lanes_merged(const Sum2x2 &a)
+{
+    return sum_merge(Sum2{lo_of(a.hi), lo_of(a.lo)}, Sum2{hi_of(a.hi), hi_of(a.lo)});
+}
+
+// Block-wide sum over `nt` threads (a multiple of 32) of the squares of their vectors `v`, of
+// which each thread has formed the compensated partial sum `acc`; rounded as the exact sum would
+// be.  `named`: synchronise only those threads on named barrier 1 (the ring kernel's consumer
 // warps); otherwise __syncthreads.  Warp partials go through `slot` / `dslot` (>= 32 entries no
 // concurrent reduction uses); every warp combines them with the same butterfly, so all threads
-// get identical bits and take the rare exact path (exact_partial(): this thread's terms summed
-// in double-double) together.
-template <typename ExactPartial>
-__device__ __forceinline__ float block_sum_w(Sum2 a, Sum2 *slot, DD *dslot, int nt, bool named,
-                                             ExactPartial exact_partial)
+// get identical bits and take the rare exact path together.
+template <int VPT>
+__device__ __forceinline__ float block_sum_sq(const Sum2x2 &acc, const uint4 (&v)[VPT],
+                                              Sum2 *slot, DD *dslot, int nt, bool named)
 {
-    a = warp_sum(a);
+    const Sum2 a = warp_sum(lanes_merged(acc));
     const int lane = threadIdx.x & 31;
     const int nw = nt >> 5;
     if (lane == 0)
@@ -96,116 +112,90 @@ __device__ __forceinline__ float block_sum_w(Sum2 a, Sum2 *slot, DD *dslot, int 
     if (!near_tie(p.hi, p.lo, r1))
         return r1;
     // rare: the row sum is within the compensated sum's error of an FP32 rounding boundary
-    return block_sum_exact(exact_partial(), dslot, nt, named);
+    return block_sum_exact(v, dslot, nt, named);
 }
 
-// This thread's squares of packed BF16 vectors, summed in double-double (the exact path).
-template <int VPT>
-__device__ __forceinline__ DD squares_dd(const uint4 (&v)[VPT])
+// b = bf16(x / s) by IEEE division for one vector of BF16 values: the rare path of the residual
+// operand (an element below the exponent floor, or a residual index whose product rule fails).
+__device__ __forceinline__ uint4 residual_operand_ieee(uint4 xh, float s)
 {
-    DD d = {0.0, 0.0};
+    uint4 b;
 #pragma unroll
-    for (int i = 0; i < VPT; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const f2 x = widen(word(v[i], j));
-            d = dd_add(d, (double)__fmul_rn(lo_of(x), lo_of(x)));
-            d = dd_add(d, (double)__fmul_rn(hi_of(x), hi_of(x)));
-        }
-    return d;
-}
-
-__device__ __forceinline__ Sum2 lanes_merged(const Sum2x2 &a)
-{
-    return sum_merge(Sum2{lo_of(a.hi), lo_of(a.lo)}, Sum2{hi_of(a.hi), hi_of(a.lo)});
-}
-
-// True when every BF16 element in `w` has |w| < 2^120, so that xhat = bf16((x r) w) cannot
-// overflow and the Markstein division step is safe for it.
-template <int N>
-__device__ __forceinline__ bool weights_small(const uint4 (&w)[N])
-{
-    constexpr uint32_t kCeil = (kWeightMaxExp << 7) | (kWeightMaxExp << 23);
-    uint32_t any = 0u;
-#pragma unroll
-    for (int i = 0; i < N; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            any |= ((word(w[i], j) & 0x7f807f80u) | 0x80008000u) - kCeil;
-    return (any & 0x80008000u) == 0u;
+    for (int j = 0; j < 4; ++j) {
+        const f2 q = widen(word(xh, j));
+        word(b, j) = narrow(make_f2(__fdiv_rn(lo_of(q), s), __fdiv_rn(hi_of(q), s)));
+    }
+    return b;
 }
 
 // The boundary chain for one row whose inputs sit in registers: xv (x) and hv (h) hold this
 // thread's vectors tid + i * nt.  wpo(i) / wpr(i) give the matching weight vectors.
-// `after_first_sum` runs right after the first block reduction.  `fast_div`: this thread may
-// use the Markstein step for x_hat / s (n small enough and its weights small).
+// `after_first_sum` runs right after the first block reduction.
 template <int VPT, typename WPost, typename WPre, typename AfterFirstSum>
 __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t row,
                                                const uint4 (&xv)[VPT], const uint4 (&hv)[VPT],
-                                               WPost wpo, WPre wpr, bool fast_div,
-                                               Sum2 (*red)[32], DD (*dred)[32], int nt,
-                                               bool named, AfterFirstSum after_first_sum)
+                                               WPost wpo, WPre wpr, Sum2 (*red)[32],
+                                               DD (*dred)[32], int nt, bool named,
+                                               AfterFirstSum after_first_sum)
 {
     const int nvec = a.H >> 3;
     const int tid = threadIdx.x;
     const int64_t row_off = row * (int64_t)a.H;
 
     // ---- a1: r = 1/sqrt(mean(x^2) + eps) ---------------------------------------------------
-    Sum2x2 acc = {0ull, 0ull};
+    // two accumulators (even / odd words) halve the dependent chain of the running sums
+    Sum2x2 acc0 = {0ull, 0ull}, acc1 = {0ull, 0ull};
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const f2 x = widen(word(xv[i], j));
-            sum2_add(acc, mul2(x, x));
+            sum2_add(j & 1 ? acc1 : acc0, mul2(x, x));
         }
     }
-    const float r = rms_inv(
-        block_sum_w(lanes_merged(acc), red[0], dred[0], nt, named, [&] { return squares_dd(xv); }),
-        (float)a.H, a.eps);
+    const float r = rms_inv(block_sum_sq(sum2_merge(acc0, acc1), xv, red[0], dred[0], nt, named),
+                            (float)a.H, a.eps);
     after_first_sum();
 
     // ---- a1 / a2: xhat = bf16((x r) w_post); h' = bf16(bf16(alpha h) + bf16(xhat / s)) -----
-    const f2 rr = splat(r), al = splat(a.alpha), ys = splat(a.inv_s), ns = splat(-a.s);
+    const f2 rr = splat(r), al = splat(a.alpha), ys = splat(a.inv_s);
+    const uint32_t floor_bits = a.floor_bits;
+    const uint32_t mul_ok = a.mul_div ? 0xffffffffu : 0u;
     uint4 hp[VPT];
-    acc = {0ull, 0ull};
+    acc0 = {0ull, 0ull};
+    acc1 = {0ull, 0ull};
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int v = tid + i * nt;
         hp[i] = make_uint4(0u, 0u, 0u, 0u);
         if (v < nvec) {
             const uint4 w = wpo(i);
-            uint32_t xh[4], bw[4];
-            uint32_t floor_all = 0xffffffffu;
+            uint4 xh, bw;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                xh[j] = narrow(mul2(mul2(widen(word(xv[i], j)), rr), widen(word(w, j))));
-                exp_floor_check(floor_all, xh[j]);
-            }
-            if (fast_div && exp_floor_ok(floor_all)) {
+            for (int j = 0; j < 4; ++j)
+                word(xh, j) = narrow(mul2(mul2(widen(word(xv[i], j)), rr), widen(word(w, j))));
+            const uint32_t ok = mul_ok & exp_floor_bits(xh.x, floor_bits) &
+                                exp_floor_bits(xh.y, floor_bits) &
+                                exp_floor_bits(xh.z, floor_bits) & exp_floor_bits(xh.w, floor_bits);
+            if (exp_floor_ok(ok)) {  // b = bf16(x_hat y), equal to bf16(x_hat / s) here
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    bw[j] = narrow(div2_markstein(widen(xh[j]), ns, ys));
-            } else {  // zero / tiny / non-finite operands, large n or huge weights
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const f2 q = widen(xh[j]);
-                    bw[j] = narrow(make_f2(__fdiv_rn(lo_of(q), a.s), __fdiv_rn(hi_of(q), a.s)));
-                }
+                    word(bw, j) = narrow(mul2(widen(word(xh, j)), ys));
+            } else {  // zero / tiny operands, or a residual index without the product rule
+                bw = residual_operand_ieee(xh, a.s);
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t aw = narrow(mul2(al, widen(word(hv[i], j))));
-                const uint32_t hq = add_bf16x2(aw, bw[j]);  // bf16(a + b)
+                const uint32_t hq = add_bf16x2(aw, word(bw, j));  // bf16(a + b)
                 word(hp[i], j) = hq;
                 const f2 hf = widen(hq);
-                sum2_add(acc, mul2(hf, hf));
+                sum2_add(j & 1 ? acc1 : acc0, mul2(hf, hf));
             }
         }
     }
     const f2 rr2 = splat(rms_inv(
-        block_sum_w(lanes_merged(acc), red[1], dred[1], nt, named, [&] { return squares_dd(hp); }),
-        (float)a.H, a.eps));
+        block_sum_sq(sum2_merge(acc0, acc1), hp, red[1], dred[1], nt, named), (float)a.H, a.eps));
 
     // ---- a3: y = bf16((h' r') w_pre); store h' and y -----------------------------------------
     char *h_out = (char *)a.h_out + 2 * row_off;
@@ -296,7 +286,6 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
         wpo[i] = weight_vec(a.w_post, tid + i * nt, nvec);
         wpr[i] = weight_vec(a.w_pre, tid + i * nt, nvec);
     }
-    const bool fast_div = a.fast_div_n && weights_small(wpo);
     pdl_wait();
 
     for (int64_t row = blockIdx.x; row < a.T; row += gridDim.x) {
@@ -323,8 +312,8 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
             }
         }
         boundary_chain<VPT>(
-            a, row, xv, hv, [&](int i) { return wpo[i]; }, [&](int i) { return wpr[i]; },
-            fast_div, red, dred, nt, false, [] {});
+            a, row, xv, hv, [&](int i) { return wpo[i]; }, [&](int i) { return wpr[i]; }, red,
+            dred, nt, false, [] {});
     }
 }
 
@@ -343,7 +332,7 @@ constexpr int kRingHeader = 256;  // 2 x up to 16 mbarriers
 constexpr int kRingMaxStages = 16;
 
 template <int VPT, bool MOE>
-__global__ void __launch_bounds__(kRingConsumers + 32)
+__global__ void __launch_bounds__(kRingConsumers + 32, MOE ? 3 : 4)
     boundary_ring_kernel(const BoundaryArgs a, int stages)
 {
     extern __shared__ __align__(128) unsigned char dyn[];
@@ -384,14 +373,15 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
         if (tid != NC)
             return;
         pdl_wait();
-        int64_t issued = 0;
+        // unit u = chunk c of row `row`, in stage st of ring pass `pass` (u = pass * stages + st);
+        // all four advance incrementally (no 64-bit division in the loop)
+        int64_t issued = 0, row = first;
+        int st = 0, c = 0;
+        uint32_t pass = 0;
         for (int64_t u = 0; u < my_units; ++u) {
-            const int st = (int)(u % stages);
-            if (u >= stages &&
-                !mbar_wait_or_fail(&empty[st], (uint32_t)((u / stages - 1) & 1), &fail))
+            // the stage's previous use (pass - 1) must have been released by the consumers
+            if (pass > 0 && !mbar_wait_or_fail(&empty[st], (pass - 1) & 1u, &fail))
                 break;
-            const int64_t row = first + (u / VPT) * stride;
-            const int c = (int)(u % VPT);
             const int nv = nvec - c * NC < NC ? nvec - c * NC : NC;
             const uint32_t bytes = (uint32_t)nv * 16u;
             unsigned char *dst = ring + (size_t)st * stage_bytes;
@@ -405,6 +395,14 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
             bulk_g2s(dst + (size_t)KIN * kSlice, (const char *)a.h_in + (size_t)row * 2 * a.H + col,
                      bytes, &full[st]);
             issued = u + 1;
+            if (++c == VPT) {
+                c = 0;
+                row += stride;
+            }
+            if (++st == stages) {
+                st = 0;
+                ++pass;
+            }
         }
         // Before leaving, make sure none of this CTA's copies is still landing (bounded).
         for (int64_t u = issued - stages > 0 ? issued - stages : 0; u < issued; ++u)
@@ -415,18 +413,12 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
     }
 
     // ---- consumer warps ----------------------------------------------------------------------
-    bool fast_div = a.fast_div_n;
-    {
-        uint4 w[VPT];
+    if constexpr (!MOE) {
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
-            w[i] = weight_vec(a.w_post, tid + i * NC, nvec);
-            if constexpr (!MOE) {
-                wsm[i * NC + tid] = w[i];
-                wsm[(VPT + i) * NC + tid] = weight_vec(a.w_pre, tid + i * NC, nvec);
-            }
+            wsm[i * NC + tid] = weight_vec(a.w_post, tid + i * NC, nvec);
+            wsm[(VPT + i) * NC + tid] = weight_vec(a.w_pre, tid + i * NC, nvec);
         }
-        fast_div = fast_div && weights_small(w);
     }
     pdl_wait();
     const int lane = tid & 31;
@@ -435,6 +427,8 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
         if (my_rows > 0)
             routing_coeffs(a, first, c_next);
     }
+    int st = 0;          // stage of the next unit
+    uint32_t parity = 0;  // phase parity of that stage's `full` barrier for this pass
     for (int64_t i = 0; i < my_rows; ++i) {
         const int64_t row = first + i * stride;
         if constexpr (MOE) {
@@ -448,9 +442,7 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
         uint4 xv[VPT], hv[VPT];
 #pragma unroll
         for (int ch = 0; ch < VPT; ++ch) {
-            const int64_t u = i * VPT + ch;
-            const int st = (int)(u % stages);
-            (void)mbar_wait_or_fail(&full[st], (uint32_t)((u / stages) & 1), &fail);
+            (void)mbar_wait_or_fail(&full[st], parity, &fail);
             const unsigned char *stage = ring + (size_t)st * stage_bytes;
             if (ch * NC + tid < nvec) {
                 hv[ch] = *reinterpret_cast<const uint4 *>(stage + (size_t)KIN * kSlice + 16 * tid);
@@ -465,17 +457,20 @@ __global__ void __launch_bounds__(kRingConsumers + 32)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[st]);  // this warp is done with the stage
+            if (++st == stages) {
+                st = 0;
+                parity ^= 1u;
+            }
         }
         if constexpr (MOE)
             boundary_chain<VPT>(
                 a, row, xv, hv, [&](int k) { return weight_vec(a.w_post, tid + k * NC, nvec); },
-                [&](int k) { return weight_vec(a.w_pre, tid + k * NC, nvec); }, fast_div, red,
-                dred, NC, true, [] {});
+                [&](int k) { return weight_vec(a.w_pre, tid + k * NC, nvec); }, red, dred, NC,
+                true, [] {});
         else
             boundary_chain<VPT>(
                 a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
-                [&](int k) { return wsm[(VPT + k) * NC + tid]; }, fast_div, red, dred, NC, true,
-                [] {});
+                [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, dred, NC, true, [] {});
     }
     if (tid == 0 && fail)
         atomicOr(&g_fault_word, kFaultCopyTimeout);

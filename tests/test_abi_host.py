@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
+from tests._util import f32_to_bf16_nearest
 import residual_stream_norm_gb300 as rsn
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -195,21 +196,39 @@ def test_rope_cos_sin_rejects_out_of_range(lib):
 # the residual operand division (host build of the kernels' arithmetic)
 # ------------------------------------------------------------------------------------------
 
-def test_residual_quotient_equals_ieee_division_exhaustively(lib):
-    # every finite BF16 value x (subnormals and signed zeros included) and every residual index
-    # n = 1..4096: the kernels' x / s must be the IEEE (correctly rounded) FP32 quotient.
+def _bf16_values(finite_only=True):
     b = np.arange(1 << 16, dtype=np.uint32)
     x = (b << 16).view(np.float32)
-    x = x[np.isfinite(x)]
+    return x[np.isfinite(x)] if finite_only else x[~np.isnan(x)]
+
+
+def _bf16_of_ieee_quotient(x, n):
+    s = np.float32(np.sqrt(np.float64(n)))
+    return f32_to_bf16_nearest(x / s)
+
+
+def _bits(b):
+    return (b.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_residual_operand_equals_bf16_of_ieee_division_exhaustively(lib):
+    # every BF16 value x (subnormals, signed zeros and infinities included) and every residual
+    # index n = 1..4096: the kernels' b must be bf16 of the IEEE (correctly rounded) FP32
+    # quotient -- whichever of the product or the division the kernels' rule picks.
+    x = _bf16_values(finite_only=False)
     for n in range(1, 4097):
-        s = np.float32(np.sqrt(np.float64(n)))
-        q = rsn.beam_residual_quotient(x, n)
-        assert np.array_equal(q.view(np.uint32), (x / s).view(np.uint32)), n
+        b = rsn.beam_residual_operand(x, n)
+        want = _bf16_of_ieee_quotient(x, n)
+        assert np.array_equal(_bits(b), want), n
 
 
-def test_residual_quotient_large_n_and_nonfinite(lib):
-    x = np.array([1.0, -3.5, 1e-30, 7e37, np.inf, -np.inf], dtype=np.float32)
-    for n in (3, 4097, 10**6, 2**31 - 1):
-        s = np.float32(np.sqrt(np.float64(n)))
-        assert np.array_equal(rsn.beam_residual_quotient(x, n), x / s)
-    assert np.isnan(rsn.beam_residual_quotient(np.array([np.nan], np.float32), 5)).all()
+def test_residual_operand_large_n_nan_and_non_bf16_inputs(lib):
+    x = _bf16_values(finite_only=False)
+    for n in (4097, 10**5, 10**6 + 3, 2**24, 2**31 - 1):
+        b = rsn.beam_residual_operand(x, n)
+        assert np.array_equal(_bits(b), _bf16_of_ieee_quotient(x, n)), n
+    assert np.isnan(rsn.beam_residual_operand(np.array([np.nan], np.float32), 5)).all()
+    with pytest.raises(rsn.BeamError):  # 1 + 2^-20 is not a BF16 value
+        rsn.beam_residual_operand(np.array([1.0 + 2.0**-20], np.float32), 5)
+    with pytest.raises(rsn.BeamError):
+        rsn.beam_residual_operand(np.array([1.0], np.float32), 0)

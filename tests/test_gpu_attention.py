@@ -120,7 +120,8 @@ def test_gate_config(T):
     assert_bf16_close(u16(run_gate(c)), oracle_gate(c), what=f"gate T={T}")
 
 
-@pytest.mark.parametrize("nh,hd", [(1, 8), (3, 16), (48, 128), (7, 1024), (1024, 8)])
+@pytest.mark.parametrize("nh,hd", [(1, 8), (3, 16), (5, 24), (48, 128), (7, 1024), (1024, 8),
+                                   (1024, 1016)])
 def test_gate_shapes(nh, hd):
     c = bi.gate_case(T=9, n_heads=nh, D=hd, seed=nh + hd)
     assert_bf16_close(u16(run_gate(c, nh=nh, hd=hd)), oracle_gate(c, nh, hd),
