@@ -87,6 +87,15 @@ BEAM_API int beam_device_faults(uint32_t *flags, int clear);
  * arrays, and for inputs that are not BF16 values (their outputs are NaN). */
 BEAM_API int beam_residual_operand(const float *x, float *b_out, int64_t count, int32_t n);
 
+/* Host-only helper: the sum of the FP32 squares v[i] * v[i] of `count` values (BF16 values given
+ * as FP32, in host memory), rounded to FP32 exactly as the kernels' rare exact path rounds a row
+ * or head sum of squares ("Sandwich-Norm": RMSNorm in FP32): in 128-bit fixed point scaled to the
+ * largest square, then rounded once to nearest even.  NaN if a square is NaN, +inf if one is
+ * infinite or the sum overflows, 0 if all are zero.  The result is the exact rounding unless some
+ * square lies more than 2^88 below the largest and the sum falls within 2^-98 (relative) of a
+ * rounding boundary.  Returns BEAM_ERR_INVALID_ARG for count < 0, count > 16384 or NULL arrays. */
+BEAM_API int beam_exact_square_sum(const float *v, int64_t count, float *out);
+
 /* Host-only helper: the FP32 cosine and sine that beam_qk_norm_rope_fwd uses for an FP32 rotary
  * angle, for `count` angles in host memory.  Each value is the FP32 rounding of the exact
  * cos / sin of the FP32 angle (except in rare near-tie cases), computed in FP32 pair arithmetic

@@ -19,7 +19,8 @@ import torch
 from . import _build
 
 __all__ = ["BeamError", "build", "lib", "beam_abi_version", "beam_status_str",
-           "beam_residual_scales", "beam_rope_cos_sin", "beam_residual_operand", "beam_device_faults",
+           "beam_residual_scales", "beam_rope_cos_sin", "beam_residual_operand",
+           "beam_exact_square_sum", "beam_device_faults",
            "beam_boundary_fwd", "beam_moe_combine_boundary_fwd",
            "beam_qk_norm_rope_fwd", "beam_qk_norm_ssmax_fwd", "beam_attn_gate_fwd",
            "HEAD_DIM"]
@@ -58,6 +59,7 @@ def lib() -> ctypes.CDLL:
             so.beam_residual_scales.argtypes = [i32, ctypes.POINTER(f32), ctypes.POINTER(f32)]
             so.beam_rope_cos_sin.argtypes = [vp, vp, vp, i64]
             so.beam_residual_operand.argtypes = [vp, vp, i64, i32]
+            so.beam_exact_square_sum.argtypes = [vp, i64, vp]
             so.beam_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
             so.beam_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, f32, vp, vp]
             so.beam_moe_combine_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, i64,
@@ -68,7 +70,7 @@ def lib() -> ctypes.CDLL:
                                                   i32, f32, f32, f32, vp]
             so.beam_attn_gate_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i64, vp]
             for fn in ("beam_abi_version", "beam_residual_scales", "beam_rope_cos_sin",
-                       "beam_residual_operand", "beam_device_faults",
+                       "beam_residual_operand", "beam_exact_square_sum", "beam_device_faults",
                        "beam_boundary_fwd",
                        "beam_moe_combine_boundary_fwd", "beam_qk_norm_rope_fwd",
                        "beam_qk_norm_ssmax_fwd", "beam_attn_gate_fwd"):
@@ -138,6 +140,18 @@ def beam_device_faults(clear: bool = False) -> int:
     if st != 0:
         raise BeamError("beam_device_faults", st)
     return v.value
+
+
+def beam_exact_square_sum(v) -> float:
+    """Host helper: the FP32 sum of the FP32 squares of `v` (BF16 values as float32), rounded as
+    the kernels' rare exact path rounds a row or head sum of squares."""
+    import numpy as np
+    a = np.ascontiguousarray(v, dtype=np.float32)
+    out = np.zeros(1, dtype=np.float32)
+    st = lib().beam_exact_square_sum(a.ctypes.data, a.size, out.ctypes.data)
+    if st != 0:
+        raise BeamError("beam_exact_square_sum", st)
+    return out[0]
 
 
 def beam_residual_operand(x, n: int):

@@ -20,6 +20,7 @@
 // nearly cancel.  Element arithmetic runs on packed FP32 pairs (beam_f32x2.cuh).
 
 #include "beam_device.cuh"
+#include "beam_exact.cuh"
 #include "beam_f32x2.cuh"
 #include "beam_kernels.h"
 #include "beam_sincos.cuh"
@@ -37,6 +38,56 @@ struct RopeTable {
     float inv_freq[kHalf];  // fp32(theta^(-2i/128)), formed on the host in double
 };
 
+// The rare exact path: this quad's head sum of the FP32 squares in 128-bit fixed point, rounded
+// once to FP32 (beam_exact.cuh).  Every lane of the warp calls it; the shuffles stay within quads,
+// and each quad's special cases (all zero, a NaN or infinite square) are selected only at the end
+// so that every lane takes part in every shuffle.  The lane reloads its four vectors of the head
+// from `row` (still the unnormalised input: the head is stored only after this), or uses zeros
+// for an inactive item (row == nullptr), so the hot loop keeps no raw copy alive for it; the
+// loops stay rolled, so the rare path costs little code and few registers.
+__device__ __forceinline__ float head_sum_exact(const char *row, int q)
+{
+    uint32_t mx = 0;  // bits of the quad's largest square (NaN patterns above +inf)
+#pragma unroll 1
+    for (int jj = 0; jj < 4; ++jj) {
+        const uint4 v = row ? ld_plain(row + 16 * (q + 4 * jj)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+            const f2 x = widen(word(v, pp));
+            mx = max(mx, __float_as_uint(__fmul_rn(lo_of(x), lo_of(x))) & 0x7fffffffu);
+            mx = max(mx, __float_as_uint(__fmul_rn(hi_of(x), hi_of(x))) & 0x7fffffffu);
+        }
+    }
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const bool special = mx == 0u || mx >= 0x7f800000u;
+    const uint32_t emax = special ? 1u : exact_emax(mx);
+    ExactAcc acc = {0ull, 0ull, 0u};
+    if (!special) {
+#pragma unroll 1
+        for (int jj = 0; jj < 4; ++jj) {
+            const uint4 v = row ? ld_plain(row + 16 * (q + 4 * jj)) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const f2 x = widen(word(v, pp));
+                exact_add(acc, __float_as_uint(__fmul_rn(lo_of(x), lo_of(x))), emax);
+                exact_add(acc, __float_as_uint(__fmul_rn(hi_of(x), hi_of(x))), emax);
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 1; off < 4; off <<= 1) {
+        ExactAcc o;
+        o.hi = __shfl_xor_sync(0xffffffffu, acc.hi, off);
+        o.lo = __shfl_xor_sync(0xffffffffu, acc.lo, off);
+        o.sticky = __shfl_xor_sync(0xffffffffu, acc.sticky, off);
+        exact_merge(acc, o);
+    }
+    if (special)
+        return mx == 0u ? 0.0f : __uint_as_float(mx > 0x7f800000u ? 0x7fc00000u : 0x7f800000u);
+    return exact_round(acc, emax);
+}
+
 // Work items are the (token, head) pairs of a tile of TT tokens.  A quad of lanes owns one head:
 // lane q holds the 16-byte vectors q, q+4, q+8 and q+12 of its 128 elements, so a warp load
 // reads 64 contiguous bytes per head, and the rotation partners (element i < 64 and i + 64,
@@ -44,23 +95,6 @@ struct RopeTable {
 // two-step butterfly over the quad.  The per-token factors of the tile (64 cos/sin pairs, or
 // the SSMax scale) are computed once into shared memory while the first loads are in flight;
 // the Q and K norm weights are held in shared memory as FP32.
-// The rare exact path: this quad's head sum of squares in double-double, rounded once to FP32
-// (every lane of the warp calls it; the shuffles stay within quads).
-__device__ __forceinline__ float head_sum_exact(const uint4 (&v)[4])
-{
-    DD d = {0.0, 0.0};
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-            const uint32_t w = word(v[jj], pp);
-            const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
-            d = dd_add(d, (double)__fmul_rn(lo, lo));
-            d = dd_add(d, (double)__fmul_rn(hi, hi));
-        }
-    return dd_to_float(dd_warp_sum(d, 4));
-}
-
 template <bool ROPE, int TT>
 __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, const RopeTable tab)
 {
@@ -151,31 +185,55 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
                 const int tt = tok[m];
                 const bool isq = head[m] < a.n_q;
                 f2 x[4][4];
-                Sum2x2 acc = {0ull, 0ull};
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
-                    for (int pp = 0; pp < 4; ++pp) {
+                    for (int pp = 0; pp < 4; ++pp)
                         x[jj][pp] = widen(word(v[m][jj], pp));
-                        sum2_add(acc, mul2(x[jj][pp], x[jj][pp]));
-                    }
-                Sum2 tot = sum_merge(Sum2{lo_of(acc.hi), lo_of(acc.lo)},
-                                     Sum2{hi_of(acc.hi), hi_of(acc.lo)});
+                float ms;
+                if constexpr (ROPE) {
+                    // The rotation can cancel, so an FP32 ulp of r could move an output by more
+                    // than a BF16 ulp: the head sum is rounded as the exact sum would be.
+                    Sum2x2 acc = {0ull, 0ull};
 #pragma unroll
-                for (int off = 1; off < 4; off <<= 1) {
-                    Sum2 o;
-                    o.hi = __shfl_xor_sync(0xffffffffu, tot.hi, off);
-                    o.lo = __shfl_xor_sync(0xffffffffu, tot.lo, off);
-                    tot = sum_merge(tot, o);
-                }
-                float ms = sum_value(tot);
-                const bool tie = near_tie(tot.hi, tot.lo, ms);
-                if (__any_sync(0xffffffffu, tie)) {
-                    // rare: recompute this head's sum exactly (double-double) so that its FP32
-                    // rounding is that of the exact sum; the whole warp joins the shuffles
-                    const float exact = head_sum_exact(v[m]);
-                    if (tie)
-                        ms = exact;
+                    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp)
+                            sum2_add(acc, mul2(x[jj][pp], x[jj][pp]));
+                    Sum2 tot = sum_merge(Sum2{lo_of(acc.hi), lo_of(acc.lo)},
+                                         Sum2{hi_of(acc.hi), hi_of(acc.lo)});
+#pragma unroll
+                    for (int off = 1; off < 4; off <<= 1) {
+                        Sum2 o;
+                        o.hi = __shfl_xor_sync(0xffffffffu, tot.hi, off);
+                        o.lo = __shfl_xor_sync(0xffffffffu, tot.lo, off);
+                        tot = sum_merge(tot, o);
+                    }
+                    ms = sum_value(tot);
+                    const bool tie = near_tie(tot.hi, tot.lo, ms);
+                    if (__any_sync(0xffffffffu, tie)) {
+                        // rare: recompute this head's sum exactly; the whole warp joins in
+                        const float exact = head_sum_exact(row[m], q);
+                        if (tie)
+                            ms = exact;
+                    }
+                } else {
+                    // The outputs only scale with r: a plain FP32 sum in a fixed order (per lane,
+                    // then the quad butterfly) moves them by at most one BF16 ulp.
+                    f2 s0 = 0ull, s1 = 0ull;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                        for (int pp = 0; pp < 4; ++pp) {
+                            if (pp & 1)
+                                s1 = fma2(x[jj][pp], x[jj][pp], s1);
+                            else
+                                s0 = fma2(x[jj][pp], x[jj][pp], s0);
+                        }
+                    const f2 s2 = add2(s0, s1);
+                    ms = __fadd_rn(lo_of(s2), hi_of(s2));
+                    ms = __fadd_rn(ms, __shfl_xor_sync(0xffffffffu, ms, 1));
+                    ms = __fadd_rn(ms, __shfl_xor_sync(0xffffffffu, ms, 2));
                 }
                 const f2 rr = splat(rms_inv(ms, (float)kHeadDim, a.eps));
                 const float *wrow = wsm[isq ? 0 : 1];

@@ -10,6 +10,7 @@
 
 #include "../../include/beam_boundary.h"
 #include "beam_kernels.h"
+#include "beam_exact.cuh"
 #include "beam_f32x2.cuh"
 #include "beam_sincos.cuh"
 
@@ -136,6 +137,38 @@ int beam_residual_operand(const float *x, float *b_out, int64_t count, int32_t n
         b_out[i] = beam::residual_operand_host(x[i], a.s, a.inv_s, a.mul_div, f);
     }
     return st;
+}
+
+int beam_exact_square_sum(const float *v, int64_t count, float *out)
+{
+    if (count < 0 || count > 16384 || !out || (count > 0 && !v))
+        return BEAM_ERR_INVALID_ARG;
+    uint32_t mx = 0;  // bits of the largest square (NaN above +inf)
+    for (int64_t i = 0; i < count; ++i) {
+        const float sq = v[i] * v[i];
+        uint32_t u;
+        std::memcpy(&u, &sq, sizeof u);
+        u &= 0x7fffffffu;
+        mx = u > mx ? u : mx;
+    }
+    if (mx >= 0x7f800000u) {
+        *out = mx > 0x7f800000u ? NAN : INFINITY;
+        return BEAM_OK;
+    }
+    if (mx == 0) {
+        *out = 0.0f;
+        return BEAM_OK;
+    }
+    const uint32_t emax = beam::exact_emax(mx);
+    beam::ExactAcc a{0, 0, 0};
+    for (int64_t i = 0; i < count; ++i) {
+        const float sq = v[i] * v[i];
+        uint32_t u;
+        std::memcpy(&u, &sq, sizeof u);
+        beam::exact_add(a, u, emax);
+    }
+    *out = beam::exact_round(a, emax);
+    return BEAM_OK;
 }
 
 int beam_rope_cos_sin(const float *angle, float *cos_out, float *sin_out, int64_t count)

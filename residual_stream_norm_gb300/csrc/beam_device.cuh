@@ -142,9 +142,9 @@ __device__ __forceinline__ Sum2 warp_sum(Sum2 a, int width = 32)
 // exactly computed) terms: an accumulator of m terms errs by at most m^2/2 u^2 (u = 2^-24; a
 // thread splits its n <= 64 terms over two accumulators, n^2/4 u^2 <= 2^-38) and each of at most
 // ten merge levels by about 5 u^2 more.  RN(hi + lo) is the FP32 rounding of the exact sum unless
-// hi + lo lies within that distance of a rounding boundary; near_tie() detects those rows
-// (about 2^-12 of them) so that they can be recomputed in double-double, whose error (~2^-100)
-// cannot change the rounding.
+// hi + lo lies within that distance of a rounding boundary; near_tie() detects those sums
+// (about 2^-12 of them) so that they can be recomputed exactly in integer arithmetic
+// (beam_exact.cuh).
 // ---------------------------------------------------------------------------------------------
 
 // True when RN(hi + lo) = r1 might not be the rounding of the exact sum.
@@ -161,54 +161,6 @@ __device__ __forceinline__ bool near_tie(float hi, float lo, float r1)
     const float band = __uint_as_float((e - 36u) << 23);     // >= 2^-37 r1
     const float res = __fadd_rn(__fsub_rn(hi, r1), lo);     // hi - r1 is exact
     return res > __fsub_rn(half_up, band) || res < __fsub_rn(band, half_dn);
-}
-
-// Double-double accumulator (Knuth's TwoSum in FP64) for the rare exact path.
-struct DD {
-    double hi, lo;
-};
-
-__device__ __forceinline__ DD dd_add(DD a, double t)
-{
-    const double s = __dadd_rn(a.hi, t);
-    const double bp = __dsub_rn(s, a.hi);
-    const double e = __dadd_rn(__dsub_rn(a.hi, __dsub_rn(s, bp)), __dsub_rn(t, bp));
-    return DD{s, __dadd_rn(a.lo, e)};
-}
-
-__device__ __forceinline__ DD dd_merge(DD a, DD b)
-{
-    DD r = dd_add(a, b.hi);
-    r.lo = __dadd_rn(r.lo, b.lo);
-    const double h = __dadd_rn(r.hi, r.lo);
-    return DD{h, __dsub_rn(r.lo, __dsub_rn(h, r.hi))};
-}
-
-__device__ __forceinline__ DD dd_warp_sum(DD a, int width = 32)
-{
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        if (off < width) {
-            DD o;
-            o.hi = __shfl_xor_sync(0xffffffffu, a.hi, off);
-            o.lo = __shfl_xor_sync(0xffffffffu, a.lo, off);
-            a = dd_merge(a, o);
-        }
-    }
-    return a;
-}
-
-// FP32 rounding (nearest even) of hi + lo for a renormalised pair: |lo| <= ulp(hi)/2, so lo can
-// only decide when hi is exactly a midpoint between two FP32 values.
-__device__ __forceinline__ float dd_to_float(DD a)
-{
-    float f = __double2float_rn(a.hi);
-    if (a.lo != 0.0) {
-        const float fd = __double2float_rd(a.hi), fu = __double2float_ru(a.hi);
-        if (fd != fu && a.hi == 0.5 * ((double)fd + (double)fu))
-            f = a.lo > 0.0 ? fu : fd;
-    }
-    return f;
 }
 
 // ---------------------------------------------------------------------------------------------

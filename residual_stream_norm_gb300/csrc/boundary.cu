@@ -28,6 +28,7 @@
 #include <mutex>
 
 #include "beam_device.cuh"
+#include "beam_exact.cuh"
 #include "beam_f32x2.cuh"
 #include "beam_kernels.h"
 #include "beam_tma.cuh"
@@ -41,35 +42,101 @@ namespace {
 
 constexpr int kMaxK = 16;
 
-// The rare exact path of block_sum_sq: the block's sum of squares of the threads' vectors in
-// double-double, rounded once to FP32.
+// Shared-memory slot of one warp in the rare exact path (beam_exact.cuh).
+struct ExactSlot {
+    uint64_t hi, lo;
+    uint32_t sticky, max_bits;
+};
+
+// A thread's VPT packed BF16 vectors, copied for the rare exact path.
 template <int VPT>
-__device__ __forceinline__ float block_sum_exact(const uint4 (&v)[VPT], DD *dslot, int nt,
-                                                 bool named)
+struct Vecs {
+    uint4 v[VPT];
+};
+
+// The rare exact path of block_sum_sq: the block's sum of the FP32 squares of the threads'
+// vectors in 128-bit fixed point, rounded once to FP32 (beam_exact.cuh).  The largest square of
+// the block sets the scale; integer sums are associative, so every thread gets the same bits.
+// The vectors arrive as a copy, and the loop over them stays rolled: the rare path costs little
+// code and few registers.
+template <int VPT>
+__device__ __forceinline__ float block_sum_exact(const Vecs<VPT> vv, ExactSlot *xslot, int nt,
+                                              bool named)
 {
+    const uint4 (&v)[VPT] = vv.v;
     const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int nw = nt >> 5;
-    DD d = {0.0, 0.0};
+    uint32_t mx = 0;  // bits of the largest square (NaN patterns above +inf)
+#pragma unroll 1
+    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const f2 x = widen(word(v[i], j));
+            const uint32_t a0 = __float_as_uint(__fmul_rn(lo_of(x), lo_of(x))) & 0x7fffffffu;
+            const uint32_t a1 = __float_as_uint(__fmul_rn(hi_of(x), hi_of(x))) & 0x7fffffffu;
+            mx = max(mx, max(a0, a1));
+        }
+    mx = __reduce_max_sync(0xffffffffu, mx);
+    if (lane == 0)
+        xslot[warp].max_bits = mx;
+    if (named)
+        named_sync(1, nt);
+    else
+        __syncthreads();
+    for (int w = 0; w < nw; ++w)
+        mx = max(mx, xslot[w].max_bits);
+    if (mx >= 0x7f800000u)  // a NaN or infinite square: the IEEE sum
+        return __uint_as_float(mx > 0x7f800000u ? 0x7fc00000u : 0x7f800000u);
+    if (mx == 0u)
+        return 0.0f;
+    const uint32_t emax = exact_emax(mx);
+    ExactAcc acc = {0ull, 0ull, 0u};
+#pragma unroll 1
+    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const f2 x = widen(word(v[i], j));
+            exact_add(acc, __float_as_uint(__fmul_rn(lo_of(x), lo_of(x))), emax);
+            exact_add(acc, __float_as_uint(__fmul_rn(hi_of(x), hi_of(x))), emax);
+        }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        ExactAcc o;
+        o.hi = __shfl_xor_sync(0xffffffffu, acc.hi, off);
+        o.lo = __shfl_xor_sync(0xffffffffu, acc.lo, off);
+        o.sticky = __shfl_xor_sync(0xffffffffu, acc.sticky, off);
+        exact_merge(acc, o);
+    }
+    if (lane == 0) {
+        xslot[warp].hi = acc.hi;
+        xslot[warp].lo = acc.lo;
+        xslot[warp].sticky = acc.sticky;
+    }
+    if (named)
+        named_sync(1, nt);
+    else
+        __syncthreads();
+    ExactAcc t = {0ull, 0ull, 0u};
+    for (int w = 0; w < nw; ++w)
+        exact_merge(t, ExactAcc{xslot[w].hi, xslot[w].lo, xslot[w].sticky});
+    return exact_round(t, emax);
+}
+
+// Compensated sum of the squares of this thread's VPT packed BF16 vectors: four independent
+// packed accumulators (one per word of a vector) keep the dependent chains short.
+template <int VPT>
+__device__ __forceinline__ Sum2x2 squares_sum(const uint4 (&v)[VPT])
+{
+    Sum2x2 acc[4] = {{0ull, 0ull}, {0ull, 0ull}, {0ull, 0ull}, {0ull, 0ull}};
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const f2 x = widen(word(v[i], j));
-            d = dd_add(d, (double)__fmul_rn(lo_of(x), lo_of(x)));
-            d = dd_add(d, (double)__fmul_rn(hi_of(x), hi_of(x)));
+            sum2_add(acc[j], mul2(x, x));
         }
-    d = dd_warp_sum(d);
-    if (lane == 0)
-        dslot[threadIdx.x >> 5] = d;
-    if (named)
-        named_sync(1, nt);
-    else
-        __syncthreads();
-    DD q = lane < nw ? dslot[lane] : DD{0.0, 0.0};
-    q = dd_warp_sum(q);
-    q.hi = __shfl_sync(0xffffffffu, q.hi, 0);
-    q.lo = __shfl_sync(0xffffffffu, q.lo, 0);
-    return dd_to_float(q);
+    return sum2_merge(sum2_merge(acc[0], acc[1]), sum2_merge(acc[2], acc[3]));
 }
 
 __device__ __forceinline__ Sum2 lanes_merged(const Sum2x2 &a)
@@ -80,12 +147,12 @@ __device__ __forceinline__ Sum2 lanes_merged(const Sum2x2 &a)
 // Block-wide sum over `nt` threads (a multiple of 32) of the squares of their vectors `v`, of
 // which each thread has formed the compensated partial sum `acc`; rounded as the exact sum would
 // be.  `named`: synchronise only those threads on named barrier 1 (the ring kernel's consumer
-// warps); otherwise __syncthreads.  Warp partials go through `slot` / `dslot` (>= 32 entries no
+// warps); otherwise __syncthreads.  Warp partials go through `slot` / `xslot` (>= 32 entries no
 // concurrent reduction uses); every warp combines them with the same butterfly, so all threads
 // get identical bits and take the rare exact path together.
 template <int VPT>
 __device__ __forceinline__ float block_sum_sq(const Sum2x2 &acc, const uint4 (&v)[VPT],
-                                              Sum2 *slot, DD *dslot, int nt, bool named)
+                                              Sum2 *slot, ExactSlot *xslot, int nt, bool named)
 {
     const Sum2 a = warp_sum(lanes_merged(acc));
     const int lane = threadIdx.x & 31;
@@ -112,7 +179,49 @@ __device__ __forceinline__ float block_sum_sq(const Sum2x2 &acc, const uint4 (&v
     if (!near_tie(p.hi, p.lo, r1))
         return r1;
     // rare: the row sum is within the compensated sum's error of an FP32 rounding boundary
-    return block_sum_exact(v, dslot, nt, named);
+    Vecs<VPT> vv;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+        vv.v[i] = v[i];
+    return block_sum_exact<VPT>(vv, xslot, nt, named);
+}
+
+// Block-wide sum over `nt` threads of the squares of their vectors, in plain FP32 and a fixed
+// order (per thread, then a warp butterfly, then the warps' partials in warp order), so every
+// thread gets the same bits.  Used where the result only scales a product -- y = bf16((h' r') w):
+// a difference of an FP32 ulp or two in r' from the exact rounding can move y by at most one
+// BF16 ulp, unlike r, whose effect reaches h' through a sum that can cancel.
+template <int VPT>
+__device__ __forceinline__ float block_sum_sq_plain(const uint4 (&v)[VPT], float *slot, int nt,
+                                                    bool named)
+{
+    f2 s0 = 0ull, s1 = 0ull;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const f2 x = widen(word(v[i], j));
+            if (j & 1)
+                s1 = fma2(x, x, s1);
+            else
+                s0 = fma2(x, x, s0);
+        }
+    const f2 s2 = add2(s0, s1);
+    float t = __fadd_rn(lo_of(s2), hi_of(s2));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, off));
+    const int nw = nt >> 5;
+    if ((threadIdx.x & 31) == 0)
+        slot[threadIdx.x >> 5] = t;
+    if (named)
+        named_sync(1, nt);
+    else
+        __syncthreads();
+    t = slot[0];
+    for (int w = 1; w < nw; ++w)
+        t = __fadd_rn(t, slot[w]);
+    return t;
 }
 
 // b = bf16(x / s) by IEEE division for one vector of BF16 values: the rare path of the residual
@@ -134,8 +243,8 @@ __device__ __forceinline__ uint4 residual_operand_ieee(uint4 xh, float s)
 template <int VPT, typename WPost, typename WPre, typename AfterFirstSum>
 __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t row,
                                                const uint4 (&xv)[VPT], const uint4 (&hv)[VPT],
-                                               WPost wpo, WPre wpr, Sum2 (*red)[32],
-                                               DD (*dred)[32], int nt, bool named,
+                                               WPost wpo, WPre wpr, Sum2 *red,
+                                               ExactSlot *xred, float *pred, int nt, bool named,
                                                AfterFirstSum after_first_sum)
 {
     const int nvec = a.H >> 3;
@@ -143,18 +252,8 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
     const int64_t row_off = row * (int64_t)a.H;
 
     // ---- a1: r = 1/sqrt(mean(x^2) + eps) ---------------------------------------------------
-    // two accumulators (even / odd words) halve the dependent chain of the running sums
-    Sum2x2 acc0 = {0ull, 0ull}, acc1 = {0ull, 0ull};
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const f2 x = widen(word(xv[i], j));
-            sum2_add(j & 1 ? acc1 : acc0, mul2(x, x));
-        }
-    }
-    const float r = rms_inv(block_sum_sq(sum2_merge(acc0, acc1), xv, red[0], dred[0], nt, named),
-                            (float)a.H, a.eps);
+    const float r =
+        rms_inv(block_sum_sq(squares_sum(xv), xv, red, xred, nt, named), (float)a.H, a.eps);
     after_first_sum();
 
     // ---- a1 / a2: xhat = bf16((x r) w_post); h' = bf16(bf16(alpha h) + bf16(xhat / s)) -----
@@ -162,8 +261,6 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
     const uint32_t floor_bits = a.floor_bits;
     const uint32_t mul_ok = a.mul_div ? 0xffffffffu : 0u;
     uint4 hp[VPT];
-    acc0 = {0ull, 0ull};
-    acc1 = {0ull, 0ull};
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int v = tid + i * nt;
@@ -187,15 +284,11 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t aw = narrow(mul2(al, widen(word(hv[i], j))));
-                const uint32_t hq = add_bf16x2(aw, word(bw, j));  // bf16(a + b)
-                word(hp[i], j) = hq;
-                const f2 hf = widen(hq);
-                sum2_add(j & 1 ? acc1 : acc0, mul2(hf, hf));
+                word(hp[i], j) = add_bf16x2(aw, word(bw, j));  // bf16(a + b)
             }
         }
     }
-    const f2 rr2 = splat(rms_inv(
-        block_sum_sq(sum2_merge(acc0, acc1), hp, red[1], dred[1], nt, named), (float)a.H, a.eps));
+    const f2 rr2 = splat(rms_inv(block_sum_sq_plain(hp, pred, nt, named), (float)a.H, a.eps));
 
     // ---- a3: y = bf16((h' r') w_pre); store h' and y -----------------------------------------
     char *h_out = (char *)a.h_out + 2 * row_off;
@@ -274,8 +367,9 @@ template <int VPT, bool MOE>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
     boundary_rows_kernel(const BoundaryArgs a)
 {
-    __shared__ Sum2 red[2][32];
-    __shared__ DD dred[2][32];
+    __shared__ Sum2 red[32];
+    __shared__ ExactSlot xred[32];
+    __shared__ float pred[32];
     const int nvec = a.H >> 3;
     const int tid = threadIdx.x;
     const int nt = blockDim.x;
@@ -313,7 +407,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
         }
         boundary_chain<VPT>(
             a, row, xv, hv, [&](int i) { return wpo[i]; }, [&](int i) { return wpr[i]; }, red,
-            dred, nt, false, [] {});
+            xred, pred, nt, false, [] {});
     }
 }
 
@@ -339,8 +433,9 @@ __global__ void __launch_bounds__(kRingConsumers + 32, MOE ? 3 : 4)
     uint64_t *full = reinterpret_cast<uint64_t *>(dyn);
     uint64_t *empty = full + kRingMaxStages;
     unsigned char *ring = dyn + kRingHeader;
-    __shared__ Sum2 red[2][32];
-    __shared__ DD dred[2][32];
+    __shared__ Sum2 red[32];
+    __shared__ ExactSlot xred[32];
+    __shared__ float pred[32];
     __shared__ int fail;
 
     constexpr int NC = kRingConsumers;
@@ -465,12 +560,13 @@ __global__ void __launch_bounds__(kRingConsumers + 32, MOE ? 3 : 4)
         if constexpr (MOE)
             boundary_chain<VPT>(
                 a, row, xv, hv, [&](int k) { return weight_vec(a.w_post, tid + k * NC, nvec); },
-                [&](int k) { return weight_vec(a.w_pre, tid + k * NC, nvec); }, red, dred, NC,
+                [&](int k) { return weight_vec(a.w_pre, tid + k * NC, nvec); }, red, xred, pred, NC,
                 true, [] {});
         else
             boundary_chain<VPT>(
                 a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
-                [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, dred, NC, true, [] {});
+                [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, true,
+                [] {});
     }
     if (tid == 0 && fail)
         atomicOr(&g_fault_word, kFaultCopyTimeout);

@@ -37,7 +37,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 11, names
+    assert len(names) == 12, names
     raw = ctypes.CDLL(rsn.LIB_PATH)
     for nm in names:
         assert hasattr(raw, nm), f"{nm} declared in the header but not exported"
@@ -232,3 +232,74 @@ def test_residual_operand_large_n_nan_and_non_bf16_inputs(lib):
         rsn.beam_residual_operand(np.array([1.0 + 2.0**-20], np.float32), 5)
     with pytest.raises(rsn.BeamError):
         rsn.beam_residual_operand(np.array([1.0], np.float32), 0)
+
+
+# ------------------------------------------------------------------------------------------
+# the kernels' rare exact path for sums of squares (host build of the same integer code)
+# ------------------------------------------------------------------------------------------
+
+def _as_bf16(x):
+    """float32 values rounded to BF16 (nearest even), returned as float32."""
+    bits = f32_to_bf16_nearest(np.asarray(x, dtype=np.float64)).astype(np.uint32) << 16
+    return bits.view(np.float32)
+
+
+def _check_exact_square_sum(v):
+    v = np.asarray(v, dtype=np.float32)
+    got = rsn.beam_exact_square_sum(v)
+    with np.errstate(over="ignore", invalid="ignore"):
+        want = oracle.exact_sum_f32(v * v)
+    if np.isnan(want):
+        assert np.isnan(got)
+    else:
+        assert np.float32(got).view(np.uint32) == np.float32(want).view(np.uint32), (got, want)
+
+
+def test_exact_square_sum_matches_exact_rounding_on_beam_rows(lib):
+    # rows like the boundary's inputs: N(0,1) * s_t, s_t ~ U(0.5, 4), some with x16 outliers
+    g = np.random.default_rng(11)
+    for k in range(400):
+        n = int(g.choice([128, 5120, 16384]))
+        v = g.standard_normal(n) * g.uniform(0.5, 4.0)
+        if k % 7 == 0:
+            v[g.integers(0, n, 4)] *= 16.0
+        _check_exact_square_sum(_as_bf16(v))
+
+
+def test_exact_square_sum_wide_ranges_tiny_and_huge(lib):
+    g = np.random.default_rng(12)
+    for k in range(200):
+        n = int(g.integers(1, 600))
+        e = g.integers(-70, 64, n) if k % 2 else g.integers(-20, 20, n)  # squares 2^-140 .. 2^128
+        v = np.ldexp(g.uniform(1.0, 2.0, n), e) * g.choice([-1.0, 1.0], n)
+        _check_exact_square_sum(_as_bf16(v))
+    # subnormal squares and subnormal sums
+    _check_exact_square_sum(_as_bf16(np.ldexp(np.ones(37), -70)))
+    _check_exact_square_sum(_as_bf16(np.ldexp(g.uniform(1, 2, 300), -66)))
+    # overflow of a square and of the sum
+    _check_exact_square_sum(np.array([2.0 ** 64, 1.0], np.float32))
+    _check_exact_square_sum(_as_bf16(np.full(5120, 2.0 ** 63)))
+    # zeros, NaN, one element
+    _check_exact_square_sum(np.zeros(17, np.float32))
+    _check_exact_square_sum(np.array([1.0, np.nan, 2.0], np.float32))
+    _check_exact_square_sum(np.array([-3.0], np.float32))
+    assert rsn.beam_exact_square_sum(np.zeros(0, np.float32)) == 0.0
+
+
+def test_exact_square_sum_rounds_ties_to_even_and_breaks_them_with_tiny_terms(lib):
+    # 1 + 2^-24 is the midpoint between 1 and 1 + 2^-23: ties to even (1.0)
+    assert rsn.beam_exact_square_sum(np.array([1.0, 2.0 ** -12], np.float32)) == 1.0
+    # a term far below the accumulator's range still breaks the tie upwards (sticky)
+    up = np.float32(1.0 + 2.0 ** -23)
+    for tiny in (2.0 ** -30, 2.0 ** -50, 2.0 ** -70):
+        v = np.array([1.0, 2.0 ** -12, tiny], np.float32)
+        assert rsn.beam_exact_square_sum(v) == up, tiny
+        _check_exact_square_sum(v)
+    # 1 + 3 * 2^-24 is the midpoint above 1 + 2^-23 (odd): ties to even rounds up
+    v = np.array([1.0, 2.0 ** -12, 2.0 ** -12, 2.0 ** -12], np.float32)
+    _check_exact_square_sum(v)
+
+
+def test_exact_square_sum_argument_checks(lib):
+    with pytest.raises(rsn.BeamError):
+        rsn.beam_exact_square_sum(np.zeros(16385, np.float32))
