@@ -274,10 +274,13 @@ def measured_peak() -> tuple[float, str]:
 
 
 def source_hash(name: str) -> str:
-    path = os.path.join(ROOT, "residual_stream_norm_gb300", "csrc", SOURCES[name])
-    h = hashlib.sha256(open(path, "rb").read())
-    dev = os.path.join(ROOT, "residual_stream_norm_gb300", "csrc", "beam_device.cuh")
-    h.update(open(dev, "rb").read())
+    """Digest of a kernel's source file and every header of the library (any change to them
+    makes the committed DRAM counters stale)."""
+    csrc = os.path.join(ROOT, "residual_stream_norm_gb300", "csrc")
+    h = hashlib.sha256(open(os.path.join(csrc, SOURCES[name]), "rb").read())
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
