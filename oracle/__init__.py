@@ -71,9 +71,16 @@ def lib() -> ctypes.CDLL:
             so.orc_qk_norm_ssmax.argtypes = [u16p, u16p, i64, i64, u16p, u16p, i64p, i64, i32,
                                              i32, i32, f32, f32, f32, f32p]
             so.orc_attn_gate.argtypes = [u16p, u16p, u16p, f32p, i64, i32, i32, i64, i64, i64]
+            u8 = ctypes.c_uint8
+            so.orc_fp8_e4m3_rne.argtypes = [f32]
+            so.orc_fp8_e4m3_rne.restype = u8
+            so.orc_fp8_e4m3_to_f32.argtypes = [u8]
+            so.orc_fp8_e4m3_to_f32.restype = f32
+            so.orc_kv_cache_write.argtypes = [ctypes.c_void_p, ctypes.c_void_p, u16p, u16p, i64,
+                                              i64, i64p, i64, i32, i32, i64, i32, f32, f32]
             for fn in ("orc_bf16_rne_array", "orc_residual_scales", "orc_rope_inv_freq",
                        "orc_boundary", "orc_moe_combine_boundary", "orc_qk_norm_rope",
-                       "orc_qk_norm_ssmax", "orc_attn_gate"):
+                       "orc_qk_norm_ssmax", "orc_attn_gate", "orc_kv_cache_write"):
                 getattr(so, fn).restype = None
             _lib = so
     return _lib
@@ -214,6 +221,37 @@ def qk_norm_ssmax(q, k, wq, wk, pos, eps: float = 1e-6, base: float = 2048.0,
                             _ptr(pos, ctypes.c_int64), T, nq, nk, D, eps, base, expo,
                             _ptr(work, ctypes.c_float))
     return q, k
+
+
+def fp8_e4m3_rne(x: float) -> int:
+    """FP32 -> FP8 E4M3 code (round to nearest even, saturating to +-448, NaN -> 0x7f)."""
+    return int(lib().orc_fp8_e4m3_rne(float(x)))
+
+
+def fp8_e4m3_to_f32(code: int) -> float:
+    """Value of an FP8 E4M3 code."""
+    return float(lib().orc_fp8_e4m3_to_f32(int(code)))
+
+
+def kv_cache_write(k_cache, v_cache, k, v, slot_mapping, cache_dtype: int = 0,
+                   k_scale: float = 1.0, v_scale: float = 1.0):
+    """Writes K' rows k [T, nk, D] and V rows v [T, nk, D] (uint16 BF16) into the slots
+    slot_mapping [T] of the caches [num_slots, nk, D]: uint16 for cache_dtype 0 (BF16), uint8
+    for cache_dtype 1 (FP8 E4M3 of value / scale).  Negative or out-of-range slots are skipped.
+    Returns new (k_cache, v_cache)."""
+    k, v = _u16(k), _u16(v)
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    T, nk, D = k.shape
+    assert v.shape == (T, nk, D) and slots.shape == (T,)
+    dt = np.uint16 if cache_dtype == 0 else np.uint8
+    kc = np.array(k_cache, dtype=dt, copy=True)
+    vc = np.array(v_cache, dtype=dt, copy=True)
+    assert kc.shape == vc.shape and kc.shape[1:] == (nk, D)
+    u = ctypes.c_uint16
+    lib().orc_kv_cache_write(kc.ctypes.data, vc.ctypes.data, _ptr(k, u), _ptr(v, u), nk * D,
+                             nk * D, _ptr(slots, ctypes.c_int64), T, nk, D, kc.shape[0],
+                             cache_dtype, k_scale, v_scale)
+    return kc, vc
 
 
 def attn_gate(attn, gate, bias, n_heads: int, head_dim: int):

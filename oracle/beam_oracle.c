@@ -378,6 +378,82 @@ void orc_qk_norm_ssmax(uint16_t *q, uint16_t *k, int64_t q_stride, int64_t k_str
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* KV-cache write (the step the Q/K kernel takes over)                                          */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Value of an FP8 E4M3 code (OCP "E4M3FN": 1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; exponent field 0 holds the subnormals m * 2^-9; S.1111.111 is NaN; no infinities). */
+float orc_fp8_e4m3_to_f32(uint8_t b)
+{
+    int e = (b >> 3) & 0xf, m = b & 7;
+    float mag;
+    if (e == 0xf && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexpf((float)m, -9);
+    else
+        mag = ldexpf(1.0f + (float)m / 8.0f, e - 7);
+    return (b & 0x80) ? -mag : mag;
+}
+
+/* FP32 -> FP8 E4M3, round to nearest even, saturating: the nearest of the finite codes, ties to
+ * the code with an even mantissa; magnitudes from 448 up (infinity included) give +-448; NaN
+ * gives 0x7f.  Written as a search over the 127 non-negative finite codes, so that it follows
+ * the format's definition directly. */
+uint8_t orc_fp8_e4m3_rne(float x)
+{
+    if (isnan(x))
+        return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    float a = fabsf(x);
+    if (a >= 448.0f)
+        return sign | 0x7e;
+    uint8_t lo = 0;                      /* largest code whose value is <= a */
+    for (uint8_t c = 1; c <= 0x7e; ++c)
+        if (orc_fp8_e4m3_to_f32(c) <= a)
+            lo = c;
+    uint8_t hi = (uint8_t)(lo + 1);      /* next code up (values grow with the code) */
+    float vlo = orc_fp8_e4m3_to_f32(lo), vhi = orc_fp8_e4m3_to_f32(hi);
+    double dlo = (double)a - (double)vlo, dhi = (double)vhi - (double)a;  /* exact in double */
+    uint8_t pick = dlo < dhi ? lo : (dhi < dlo ? hi : ((lo & 1) ? hi : lo));
+    return sign | pick;
+}
+
+/* Writes one token's K' rows and V rows into the paged caches, as a separate cache-write kernel
+ * would after the Q/K norm: for each token t with slot s = slot_mapping[t] in [0, num_slots),
+ *   k_cache[s, h, :] = K'[t, h, :]   and   v_cache[s, h, :] = V[t, h, :]      (h < nk)
+ * in BF16 (cache_dtype 0: the bits as they are) or in FP8 E4M3 (cache_dtype 1:
+ * fp8(bf16 value / scale), FP32 division, one scale per cache).  Tokens with a negative or
+ * out-of-range slot are skipped.  Caches are [num_slots, nk, D] (1 or 2 bytes per element).
+ * [vLLM] "MoE und Residual-Stream", change 6 (the Q/K-norm and RoPE kernel also writes K and V
+ * into the KV cache); the serving command's FP8 KV cache; [SGL] "目标模型与草稿模型 KV 的统一内存"
+ * (KV writes go to the physical slot of each token). */
+void orc_kv_cache_write(void *k_cache, void *v_cache, const uint16_t *k, const uint16_t *v,
+                        int64_t k_stride, int64_t v_stride, const int64_t *slot_mapping,
+                        int64_t T, int32_t nk, int32_t D, int64_t num_slots, int32_t cache_dtype,
+                        float k_scale, float v_scale)
+{
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t s = slot_mapping[t];
+        if (s < 0 || s >= num_slots)
+            continue;
+        for (int32_t h = 0; h < nk; ++h)
+            for (int32_t d = 0; d < D; ++d) {
+                int64_t src_k = t * k_stride + (int64_t)h * D + d;
+                int64_t src_v = t * v_stride + (int64_t)h * D + d;
+                int64_t dst = (s * nk + h) * (int64_t)D + d;
+                if (cache_dtype == 0) {
+                    ((uint16_t *)k_cache)[dst] = k[src_k];
+                    ((uint16_t *)v_cache)[dst] = v[src_v];
+                } else {
+                    ((uint8_t *)k_cache)[dst] = orc_fp8_e4m3_rne(orc_bf16_to_f32(k[src_k]) / k_scale);
+                    ((uint8_t *)v_cache)[dst] = orc_fp8_e4m3_rne(orc_bf16_to_f32(v[src_v]) / v_scale);
+                }
+            }
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* Sigmoid attention-output gate                                                               */
 /* ------------------------------------------------------------------------------------------ */
 
