@@ -150,6 +150,22 @@ def attn_qk_case(T: int, n_q: int = N_Q_HEADS, n_kv: int = N_KV_HEADS, D: int = 
     return dict(q=q, k=k, wq=wq, wk=wk, pos=torch.from_numpy(pos), eps=EPS)
 
 
+def kv_cache_case(T: int, n_kv: int = N_KV_HEADS, D: int = HEAD_DIM, slots_per_token: int = 4,
+                  pad_frac: float = 0.05, oob_frac: float = 0.02, seed: int = 0) -> dict:
+    """V [T, n_kv, D] ~ N(0, 1) and a slot mapping into a paged cache of
+    ``num_slots = slots_per_token * T`` slots: each token gets a distinct random slot, except a
+    ``pad_frac`` share of padding tokens (slot -1) and an ``oob_frac`` share mapped past the end
+    of the cache (which must not be written)."""
+    g = rng(seed)
+    v = to_bf16(normal(g, (T, n_kv, D)))
+    num_slots = slots_per_token * T
+    slots = g.permutation(num_slots)[:T].astype(np.int64)
+    u = g.random(T)
+    slots[u < pad_frac] = -1
+    slots[(u >= pad_frac) & (u < pad_frac + oob_frac)] = num_slots + g.integers(0, 1000)
+    return dict(v=v, slot_mapping=torch.from_numpy(slots), num_slots=num_slots)
+
+
 def gate_case(T: int, n_heads: int = N_Q_HEADS, D: int = HEAD_DIM, seed: int = 0) -> dict:
     """attn ~ N(0, 1); gate ~ N(0, 2) read as variance 2 (std sqrt 2); per-head bias ~ N(0, 1)
     in FP32."""

@@ -52,6 +52,9 @@ BYTES_PER_TOKEN = {
     "moe_combine_boundary": (K + 1) * H * 2 + 2 * H * 2 + K * 4,  # experts, h; h', y; weights
 }
 KERNELS = list(BYTES_PER_TOKEN)
+# Rows beyond the five-kernel step, timed alone: the Q/K kernels fused with the KV-cache write
+# (V read, slot read, K' and V rows written as FP8 E4M3, 1 byte per element).
+KV_BYTES_PER_TOKEN = BYTES_PER_TOKEN["qk_norm_rope"] + NKV * D * 2 + 8 + 2 * NKV * D
 SOURCES = {
     "qk_norm_rope": "attention.cu", "qk_norm_ssmax": "attention.cu", "attn_gate": "attention.cu",
     "boundary": "boundary.cu", "moe_combine_boundary": "boundary.cu",
@@ -376,6 +379,48 @@ def decode_chain_us(device, replays: int = 200) -> dict:
             "T": 1, "note": "working set fits in L2: time only, no HBM GB/s"}
 
 
+def kv_cache_rows(host: dict, device, peak: float, iters: int = 50) -> dict:
+    """The Q/K kernels fused with an FP8 KV-cache write at the step's T, each launch timed alone
+    with CUDA events (inputs larger than L2)."""
+    import residual_stream_norm_gb300 as rsn
+    T = host["q_r"].shape[0]
+    kv = bi.kv_cache_case(T=T, pad_frac=0.0, oob_frac=0.0, seed=7)
+    d = {k: host[k].to(device) for k in ("q_r", "k_r", "pos_r", "wq_r", "wk_r", "q_s", "k_s",
+                                         "pos_s", "wq_s", "wk_s")}
+    v = kv["v"].to(device)
+    slots = kv["slot_mapping"].to(device)
+    kc = torch.zeros((kv["num_slots"], NKV, D), dtype=torch.uint8, device=device)
+    vc = torch.zeros_like(kc)
+    runs = {
+        "qk_norm_rope_kv_fp8": lambda: rsn.beam_qk_norm_rope_kv_fwd(
+            d["q_r"], d["k_r"], v, d["wq_r"], d["wk_r"], d["pos_r"], slots, kc, vc,
+            cache_dtype=rsn.CACHE_FP8_E4M3),
+        "qk_norm_ssmax_kv_fp8": lambda: rsn.beam_qk_norm_ssmax_kv_fwd(
+            d["q_s"], d["k_s"], v, d["wq_s"], d["wk_s"], d["pos_s"], slots, kc, vc,
+            cache_dtype=rsn.CACHE_FP8_E4M3),
+    }
+    out = {}
+    for name, fn in runs.items():
+        for _ in range(5):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record()
+        for _ in range(iters):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1) / iters
+        by = KV_BYTES_PER_TOKEN * T
+        gbs = by / (ms * 1e-3) / 1e9
+        out[name] = {"us": round(ms * 1e3, 2), "bytes_per_launch": by, "gb_s": round(gbs, 1),
+                     "frac_of_peak": round(gbs / peak, 4),
+                     "tokens_per_s": round(T / (ms * 1e-3), 1),
+                     "launches": iters, "cache": f"FP8 E4M3, {kv['num_slots']} slots, "
+                                                  "one distinct random slot per token"}
+    return out
+
+
 def run_gpu_arm(args) -> None:
     ws, rank, local = dist_env()
     device = torch.device("cuda", local)
@@ -457,6 +502,7 @@ def run_gpu_arm(args) -> None:
            "path": "pinned host buffers -> cudaMemcpyAsync -> C ABI -> cudaMemcpyAsync -> host"}
 
     decode = decode_chain_us(device)
+    next_rows = kv_cache_rows(host, device, peak)
 
     out = None
     if rank == 0:
@@ -479,7 +525,8 @@ def run_gpu_arm(args) -> None:
                        "l2": "inputs larger than L2 (every kernel streams >= 168 MB per launch; "
                              "L2 129 MB); no flush",
                        "parallelism": f"replicas x{ws}"},
-            "kernels": kernels, "roofline": roofline, "decode": decode, "e2e": e2e,
+            "kernels": kernels, "roofline": roofline, "decode": decode, "next": next_rows,
+            "e2e": e2e,
             "cpu_baseline": cpu, "gpu_launches": gpu_launches * ws,
             "clocks": clocks.summary(t_wall0, t_wall1),
             "wall_timed_s": round(t_wall1 - t_wall0, 4),

@@ -166,6 +166,9 @@ BEAM_API int beam_moe_combine_boundary_fwd(void *h_out, void *y_out, const void 
  *
  * Per token t and head (row v of 128 elements, weight w = wq for Q heads, wk for K heads):
  *   r = 1 / sqrt(m(v) + eps);  qhat_d = (v_d * r) * w_d   (FP32, not rounded)
+ * m(v) = fp32(sum of the FP32 squares) / 128, the sum rounded as the exact sum would be (the
+ * rotation can cancel, so an FP32 ulp of r could otherwise move an output by more than one
+ * BF16 ulp).
  *   angle_i = fp32(fp32(pos[t]) * inv_freq_i),  inv_freq_i = fp32(theta^(-2i/128)), i < 64
  *   out_i    = bf16( fp32(qhat_i * cos_i)    - fp32(qhat_{i+64} * sin_i) )
  *   out_{i+64} = bf16( fp32(qhat_{i+64} * cos_i) + fp32(qhat_i * sin_i) )
@@ -192,13 +195,55 @@ BEAM_API int beam_qk_norm_rope_fwd(void *q, void *k, int64_t q_row_stride, int64
  * p the 1-based position); [SGL] "稠密层与分组 MoE 路由", SSMax paragraph (after the Q/K norm,
  * the query at 0-based position p is scaled by (1 + (p+1)/2048)^0.1).
  *
- * Q heads: out = bf16( ((v * r) * wq) * sigma_t ),  sigma_t = fp32((1 + (pos[t]+1)/base)^expo)
- * evaluated in double and rounded once;  K heads: out = bf16( (v * r) * wk ) (no scale).
+ * Q heads: out = bf16( ((v * r) * wq) * sigma_t ),  sigma_t = powf(1 + fp32(pos[t]+1) / base, expo)
+ * (CUDA's powf, within a few FP32 ulps of the exact value);  K heads: out = bf16( (v * r) * wk )
+ * (no scale).  r as for RoPE, except that the head sum of squares is a plain FP32 sum in a fixed
+ * order: the outputs only scale with r, so an FP32 ulp moves them by at most one BF16 ulp.
  * Arguments as beam_qk_norm_rope_fwd; ssmax_base > 0 (2048), ssmax_exp finite (0.1). */
 BEAM_API int beam_qk_norm_ssmax_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride,
                            const void *wq, const void *wk, const int64_t *pos, int64_t T,
                            int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, float eps,
                            float ssmax_base, float ssmax_exp, cudaStream_t stream);
+
+/* The Q/K calls above fused with the KV-cache write of the same tokens.
+ *
+ * [vLLM] "MoE und Residual-Stream", change 6 (the Q/K-norm and RoPE kernel also writes K and V
+ * into the KV cache, so no separate cache-write kernel runs) and the serving command's FP8 KV
+ * cache; [vLLM] "Attention", bullet "Kleiner KV-Cache" (only the full-attention layers keep the
+ * whole sequence); [SGL] "目标模型与草稿模型 KV 的统一内存" (KV writes go to each token's physical
+ * slot).
+ *
+ * Q and K are normalised (and rotated, or scaled) in place exactly as by beam_qk_norm_rope_fwd /
+ * beam_qk_norm_ssmax_fwd.  In the same pass, for each token t whose slot s = slot_mapping[t]
+ * lies in [0, num_slots):
+ *   k_cache[s, h, :] = K'[t, h, :]  (the stored, normalised K)   v_cache[s, h, :] = V[t, h, :]
+ * as BF16 (cache_dtype 0: the bits) or FP8 E4M3 (cache_dtype 1: fp8(value / scale), FP32
+ * division, round to nearest even, saturating to +-448, NaN to a NaN code).  Tokens with a
+ * negative (padding) or out-of-range slot write no cache row.  Slots of one call must be
+ * distinct; if two tokens share one, which row lands is unspecified.
+ *
+ *   v [T, n_kv_heads, 128] bf16, row t at v + t*v_row_stride (elements; >= n_kv_heads*128,
+ *     multiple of 8, 16-byte aligned); read only
+ *   slot_mapping [T] int64;  k_cache, v_cache [num_slots, n_kv_heads, 128], contiguous, 2 bytes
+ *     per element (16-byte aligned) for BF16, 1 byte (8-byte aligned) for FP8; must not overlap
+ *     each other or the other arguments
+ *   k_scale, v_scale: finite and > 0 for FP8 (ignored for BF16)
+ * BEAM_ERR_UNSUPPORTED for any other cache_dtype; with n_kv_heads == 0 nothing is cached and
+ * the cache arguments may be NULL.  Other arguments and checks as the calls above. */
+BEAM_API int beam_qk_norm_rope_kv_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride,
+                             const void *v, int64_t v_row_stride, const void *wq, const void *wk,
+                             const int64_t *pos, const int64_t *slot_mapping, void *k_cache,
+                             void *v_cache, int64_t num_slots, int32_t cache_dtype, float k_scale,
+                             float v_scale, int64_t T, int32_t n_q_heads, int32_t n_kv_heads,
+                             int32_t head_dim, float eps, float theta, cudaStream_t stream);
+
+BEAM_API int beam_qk_norm_ssmax_kv_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride,
+                              const void *v, int64_t v_row_stride, const void *wq, const void *wk,
+                              const int64_t *pos, const int64_t *slot_mapping, void *k_cache,
+                              void *v_cache, int64_t num_slots, int32_t cache_dtype, float k_scale,
+                              float v_scale, int64_t T, int32_t n_q_heads, int32_t n_kv_heads,
+                              int32_t head_dim, float eps, float ssmax_base, float ssmax_exp,
+                              cudaStream_t stream);
 
 /* Sigmoid attention-output gate, before the output projection.
  *

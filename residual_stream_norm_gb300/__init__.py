@@ -22,7 +22,8 @@ __all__ = ["BeamError", "build", "lib", "beam_abi_version", "beam_status_str",
            "beam_residual_scales", "beam_rope_cos_sin", "beam_residual_operand",
            "beam_exact_square_sum", "beam_device_faults",
            "beam_boundary_fwd", "beam_moe_combine_boundary_fwd",
-           "beam_qk_norm_rope_fwd", "beam_qk_norm_ssmax_fwd", "beam_attn_gate_fwd",
+           "beam_qk_norm_rope_fwd", "beam_qk_norm_ssmax_fwd", "beam_qk_norm_rope_kv_fwd",
+           "beam_qk_norm_ssmax_kv_fwd", "beam_attn_gate_fwd",
            "HEAD_DIM"]
 
 HEAD_DIM = 128
@@ -69,11 +70,18 @@ def lib() -> ctypes.CDLL:
             so.beam_qk_norm_ssmax_fwd.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, i32, i32,
                                                   i32, f32, f32, f32, vp]
             so.beam_attn_gate_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i64, vp]
+            so.beam_qk_norm_rope_kv_fwd.argtypes = [vp, vp, i64, i64, vp, i64, vp, vp, vp, vp, vp,
+                                                    vp, i64, i32, f32, f32, i64, i32, i32, i32,
+                                                    f32, f32, vp]
+            so.beam_qk_norm_ssmax_kv_fwd.argtypes = [vp, vp, i64, i64, vp, i64, vp, vp, vp, vp,
+                                                     vp, vp, i64, i32, f32, f32, i64, i32, i32,
+                                                     i32, f32, f32, f32, vp]
             for fn in ("beam_abi_version", "beam_residual_scales", "beam_rope_cos_sin",
                        "beam_residual_operand", "beam_exact_square_sum", "beam_device_faults",
                        "beam_boundary_fwd",
                        "beam_moe_combine_boundary_fwd", "beam_qk_norm_rope_fwd",
-                       "beam_qk_norm_ssmax_fwd", "beam_attn_gate_fwd"):
+                       "beam_qk_norm_ssmax_fwd", "beam_qk_norm_rope_kv_fwd",
+                       "beam_qk_norm_ssmax_kv_fwd", "beam_attn_gate_fwd"):
                 getattr(so, fn).restype = ctypes.c_int
             _lib = so
     return _lib
@@ -259,6 +267,59 @@ def beam_qk_norm_ssmax_fwd(q, k, wq, wk, pos, eps: float = 1e-6, ssmax_base: flo
     with torch.cuda.device(q.device):
         _call("beam_qk_norm_ssmax_fwd", _ptr(q), _ptr(k), qs, ks, _ptr(wq), _ptr(wk), _ptr(pos),
               T, nq, nk, HEAD_DIM, eps, ssmax_base, ssmax_exp, _stream(stream))
+
+
+CACHE_BF16, CACHE_FP8_E4M3 = 0, 1
+
+
+def _kv_common(k, v, slot_mapping, k_cache, v_cache, cache_dtype):
+    T, nk, ks = _heads(k, "k")
+    Tv, nv, vs = _heads(v, "v")
+    if (Tv, nv) != (T, nk):
+        raise ValueError("v must have k's shape")
+    if not (isinstance(slot_mapping, torch.Tensor) and slot_mapping.dtype == torch.int64 and
+            slot_mapping.is_cuda and slot_mapping.is_contiguous() and slot_mapping.shape == (T,)):
+        raise TypeError("slot_mapping: expected a contiguous CUDA int64 tensor of shape [T]")
+    esize = 2 if cache_dtype == CACHE_BF16 else 1
+    for c, nm in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        if not (isinstance(c, torch.Tensor) and c.is_cuda and c.is_contiguous() and
+                c.element_size() == esize and c.dim() == 3 and c.shape[1:] == (nk, HEAD_DIM) and
+                (cache_dtype != CACHE_BF16 or c.dtype == torch.bfloat16)):
+            raise TypeError(f"{nm}: expected a contiguous CUDA [num_slots, {nk}, {HEAD_DIM}] "
+                            f"tensor of {esize}-byte elements")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache must have the same shape")
+    return vs, k_cache.shape[0]
+
+
+def beam_qk_norm_rope_kv_fwd(q, k, v, wq, wk, pos, slot_mapping, k_cache, v_cache,
+                             cache_dtype: int = CACHE_BF16, k_scale: float = 1.0,
+                             v_scale: float = 1.0, eps: float = 1e-6, theta: float = 10000.0,
+                             stream=None) -> None:
+    """beam_qk_norm_rope_fwd fused with the KV-cache write: K' (as stored) and v [T, nk, 128]
+    bf16 go to the slots slot_mapping [T] int64 of k_cache / v_cache [num_slots, nk, 128]:
+    bfloat16 tensors for CACHE_BF16, 1-byte tensors (uint8 or float8_e4m3fn) for
+    CACHE_FP8_E4M3 (value / scale).  Negative or out-of-range slots are skipped."""
+    T, nq, nk, qs, ks = _qk_common(q, k, wq, wk, pos)
+    vs, num_slots = _kv_common(k, v, slot_mapping, k_cache, v_cache, cache_dtype)
+    with torch.cuda.device(q.device):
+        _call("beam_qk_norm_rope_kv_fwd", _ptr(q), _ptr(k), qs, ks, _ptr(v), vs, _ptr(wq),
+              _ptr(wk), _ptr(pos), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), num_slots,
+              cache_dtype, k_scale, v_scale, T, nq, nk, HEAD_DIM, eps, theta, _stream(stream))
+
+
+def beam_qk_norm_ssmax_kv_fwd(q, k, v, wq, wk, pos, slot_mapping, k_cache, v_cache,
+                              cache_dtype: int = CACHE_BF16, k_scale: float = 1.0,
+                              v_scale: float = 1.0, eps: float = 1e-6, ssmax_base: float = 2048.0,
+                              ssmax_exp: float = 0.1, stream=None) -> None:
+    """beam_qk_norm_ssmax_fwd fused with the KV-cache write (as beam_qk_norm_rope_kv_fwd)."""
+    T, nq, nk, qs, ks = _qk_common(q, k, wq, wk, pos)
+    vs, num_slots = _kv_common(k, v, slot_mapping, k_cache, v_cache, cache_dtype)
+    with torch.cuda.device(q.device):
+        _call("beam_qk_norm_ssmax_kv_fwd", _ptr(q), _ptr(k), qs, ks, _ptr(v), vs, _ptr(wq),
+              _ptr(wk), _ptr(pos), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), num_slots,
+              cache_dtype, k_scale, v_scale, T, nq, nk, HEAD_DIM, eps, ssmax_base, ssmax_exp,
+              _stream(stream))
 
 
 def beam_attn_gate_fwd(out, attn, gate, bias, n_heads: int, head_dim: int = HEAD_DIM,

@@ -19,6 +19,8 @@
 // (beam_sincos.cuh), so the rotation matches the oracle bit for bit even where its two products
 // nearly cancel.  Element arithmetic runs on packed FP32 pairs (beam_f32x2.cuh).
 
+#include <cuda_fp8.h>
+
 #include "beam_device.cuh"
 #include "beam_exact.cuh"
 #include "beam_f32x2.cuh"
@@ -39,13 +41,13 @@ struct RopeTable {
 };
 
 // The rare exact path: this quad's head sum of the FP32 squares in 128-bit fixed point, rounded
-// once to FP32 (beam_exact.cuh).  Every lane of the warp calls it; the shuffles stay within quads,
-// and each quad's special cases (all zero, a NaN or infinite square) are selected only at the end
-// so that every lane takes part in every shuffle.  The lane reloads its four vectors of the head
+// once to FP32 (beam_exact.cuh).  Called together by the lanes of `qmask` (the quad, or the whole
+// warp); the shuffles stay within quads, and each quad's special cases (all zero, a NaN or
+// infinite square) are selected only at the end so that every lane takes part in every shuffle.  The lane reloads its four vectors of the head
 // from `row` (still the unnormalised input: the head is stored only after this), or uses zeros
 // for an inactive item (row == nullptr), so the hot loop keeps no raw copy alive for it; the
 // loops stay rolled, so the rare path costs little code and few registers.
-__device__ __forceinline__ float head_sum_exact(const char *row, int q)
+__device__ __forceinline__ float head_sum_exact(const char *row, int q, unsigned qmask)
 {
     uint32_t mx = 0;  // bits of the quad's largest square (NaN patterns above +inf)
 #pragma unroll 1
@@ -58,8 +60,8 @@ __device__ __forceinline__ float head_sum_exact(const char *row, int q)
             mx = max(mx, __float_as_uint(__fmul_rn(hi_of(x), hi_of(x))) & 0x7fffffffu);
         }
     }
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    mx = max(mx, __shfl_xor_sync(qmask, mx, 1));
+    mx = max(mx, __shfl_xor_sync(qmask, mx, 2));
     const bool special = mx == 0u || mx >= 0x7f800000u;
     const uint32_t emax = special ? 1u : exact_emax(mx);
     ExactAcc acc = {0ull, 0ull, 0u};
@@ -78,14 +80,36 @@ __device__ __forceinline__ float head_sum_exact(const char *row, int q)
 #pragma unroll
     for (int off = 1; off < 4; off <<= 1) {
         ExactAcc o;
-        o.hi = __shfl_xor_sync(0xffffffffu, acc.hi, off);
-        o.lo = __shfl_xor_sync(0xffffffffu, acc.lo, off);
-        o.sticky = __shfl_xor_sync(0xffffffffu, acc.sticky, off);
+        o.hi = __shfl_xor_sync(qmask, acc.hi, off);
+        o.lo = __shfl_xor_sync(qmask, acc.lo, off);
+        o.sticky = __shfl_xor_sync(qmask, acc.sticky, off);
         exact_merge(acc, o);
     }
     if (special)
         return mx == 0u ? 0.0f : __uint_as_float(mx > 0x7f800000u ? 0x7fc00000u : 0x7f800000u);
     return exact_round(acc, emax);
+}
+
+// One 8-element vector of BF16 values `o` into a KV cache at element offset `e`: the BF16 bits
+// (mode 1), or FP8 E4M3 of value / scale (mode 2; round to nearest even, saturating).  The
+// quotient is IEEE division, or a product by the exact reciprocal where the scale is a power of
+// two (the same value).
+__device__ __forceinline__ void cache_store(void *cache, int64_t e, uint4 o, int mode, float scale,
+                                            float inv, bool pow2)
+{
+    if (mode == 1) {
+        st_global((char *)cache + 2 * e, o);
+        return;
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const f2 x = widen(word(o, j));
+        const float lo = pow2 ? __fmul_rn(lo_of(x), inv) : __fdiv_rn(lo_of(x), scale);
+        const float hi = pow2 ? __fmul_rn(hi_of(x), inv) : __fdiv_rn(hi_of(x), scale);
+        w[j] = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+    }
+    st_global_v2((char *)cache + e, w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
 // Work items are the (token, head) pairs of a tile of TT tokens.  A quad of lanes owns one head:
@@ -94,15 +118,22 @@ __device__ __forceinline__ float head_sum_exact(const char *row, int q)
 // i.e. vectors q and q+8, q+4 and q+12) sit in the same lane.  The head's sum of squares needs a
 // two-step butterfly over the quad.  The per-token factors of the tile (64 cos/sin pairs, or
 // the SSMax scale) are computed once into shared memory while the first loads are in flight;
-// the Q and K norm weights are held in shared memory as FP32.
-template <bool ROPE, int TT>
+// the Q and K norm weights are held in shared memory as FP32.  With a KV cache the items also
+// include the V heads: their rows go to the V cache as they are, and the K rows go to the K
+// cache as they are stored (after the norm and rotation), in the same pass.  Quads of one warp
+// may then take different paths, so every shuffle is masked to its quad.
+template <bool ROPE, int TT, bool KV>
 __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, const RopeTable tab)
 {
     __shared__ __align__(16) float cs[2][TT][kHalf];  // double-buffered by tile parity
     __shared__ __align__(16) float sn[2][TT][kHalf];
     __shared__ float scale_q[2][TT];
     __shared__ __align__(16) float wsm[2][kHeadDim];  // wq, wk as FP32
-    const int nheads = a.n_q + a.n_kv;
+    const int nqk = a.n_q + a.n_kv;
+    const int nheads = nqk + (KV ? a.n_kv : 0);  // Q, K, then V heads
+    // shuffles: masked to the quad when V items may send quads of a warp different ways,
+    // warp-wide otherwise
+    const unsigned qmask = KV ? 0xfu << (threadIdx.x & 28) : 0xffffffffu;
     const int tid = threadIdx.x;
     const int q = tid & 3;
     const int slot = tid >> 2;
@@ -145,10 +176,14 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
                     v[m][jj] = zero;
                 if (j < nitems) {
                     const int64_t t = t0 + tt;
-                    row[m] = hd < a.n_q
-                                 ? (char *)a.q + 2 * (t * a.q_stride + (int64_t)hd * kHeadDim)
-                                 : (char *)a.k +
-                                       2 * (t * a.k_stride + (int64_t)(hd - a.n_q) * kHeadDim);
+                    if (hd < a.n_q)
+                        row[m] = (char *)a.q + 2 * (t * a.q_stride + (int64_t)hd * kHeadDim);
+                    else if (hd < nqk)
+                        row[m] = (char *)a.k +
+                                 2 * (t * a.k_stride + (int64_t)(hd - a.n_q) * kHeadDim);
+                    else  // V rows are only read
+                        row[m] = (char *)a.v +
+                                 2 * (t * a.v_stride + (int64_t)(hd - nqk) * kHeadDim);
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj)
                         v[m][jj] = ld_plain(row[m] + 16 * (q + 4 * jj));
@@ -184,6 +219,22 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
                 const bool act = row[m] != nullptr;  // uniform across each quad
                 const int tt = tok[m];
                 const bool isq = head[m] < a.n_q;
+                // the cache slot of a K or V item (-1: no cache, padding or out of range)
+                int64_t cslot = -1;
+                if (KV && act && !isq) {
+                    const int64_t s = a.slot[t0 + tt];
+                    cslot = s >= 0 && s < a.num_slots ? s : -1;
+                }
+                if (KV && head[m] >= nqk) {  // a V item: into the V cache, unchanged
+                    if (cslot >= 0) {
+                        const int64_t e0 = (cslot * a.n_kv + (head[m] - nqk)) * kHeadDim;
+#pragma unroll
+                        for (int jj = 0; jj < 4; ++jj)
+                            cache_store(a.v_cache, e0 + 8 * (q + 4 * jj), v[m][jj], a.cache_mode,
+                                        a.v_scale, a.v_inv, a.v_pow2);
+                    }
+                    continue;
+                }
                 f2 x[4][4];
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
@@ -205,15 +256,18 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
 #pragma unroll
                     for (int off = 1; off < 4; off <<= 1) {
                         Sum2 o;
-                        o.hi = __shfl_xor_sync(0xffffffffu, tot.hi, off);
-                        o.lo = __shfl_xor_sync(0xffffffffu, tot.lo, off);
+                        o.hi = __shfl_xor_sync(qmask, tot.hi, off);
+                        o.lo = __shfl_xor_sync(qmask, tot.lo, off);
                         tot = sum_merge(tot, o);
                     }
                     ms = sum_value(tot);
-                    const bool tie = near_tie(tot.hi, tot.lo, ms);
-                    if (__any_sync(0xffffffffu, tie)) {
-                        // rare: recompute this head's sum exactly; the whole warp joins in
-                        const float exact = head_sum_exact(row[m], q);
+                    const bool tie = near_tie(tot.hi, tot.lo, ms);  // the same in the quad
+                    if constexpr (KV) {
+                        if (tie)  // rare
+                            ms = head_sum_exact(row[m], q, qmask);
+                    } else if (__any_sync(0xffffffffu, tie)) {
+                        // rare; the whole warp joins the (warp-wide) shuffles
+                        const float exact = head_sum_exact(row[m], q, qmask);
                         if (tie)
                             ms = exact;
                     }
@@ -232,8 +286,8 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
                         }
                     const f2 s2 = add2(s0, s1);
                     ms = __fadd_rn(lo_of(s2), hi_of(s2));
-                    ms = __fadd_rn(ms, __shfl_xor_sync(0xffffffffu, ms, 1));
-                    ms = __fadd_rn(ms, __shfl_xor_sync(0xffffffffu, ms, 2));
+                    ms = __fadd_rn(ms, __shfl_xor_sync(qmask, ms, 1));
+                    ms = __fadd_rn(ms, __shfl_xor_sync(qmask, ms, 2));
                 }
                 const f2 rr = splat(rms_inv(ms, (float)kHeadDim, a.eps));
                 const float *wrow = wsm[isq ? 0 : 1];
@@ -278,6 +332,8 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
                             out[jj][pp] = isq ? mul2(qh[jj][pp], sc) : qh[jj][pp];
                 }
                 if (act) {
+                    const int64_t e0 =
+                        KV && cslot >= 0 ? (cslot * a.n_kv + (head[m] - a.n_q)) * kHeadDim : 0;
 #pragma unroll
                     for (int jj = 0; jj < 4; ++jj) {
                         uint4 o;
@@ -285,6 +341,9 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
                         for (int pp = 0; pp < 4; ++pp)
                             word(o, pp) = narrow(out[jj][pp]);
                         st_global(row[m] + 16 * (q + 4 * jj), o);
+                        if (KV && cslot >= 0)  // a K item: the stored K' also into the K cache
+                            cache_store(a.k_cache, e0 + 8 * (q + 4 * jj), o, a.cache_mode,
+                                        a.k_scale, a.k_inv, a.k_pow2);
                     }
                 }
             }
@@ -351,7 +410,7 @@ inline unsigned grid_for(int64_t units)
     return (unsigned)(units < (int64_t)(1 << 30) ? units : (int64_t)(1 << 30));
 }
 
-template <bool ROPE>
+template <bool ROPE, bool KV>
 cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
 {
     RopeTable tab;
@@ -360,10 +419,10 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
     // Few tokens: one token per CTA spreads them over more SMs; otherwise two per CTA.
     const cudaError_t e =
         a.T < 2 * 152
-            ? launch_pdl(qk_norm_kernel<ROPE, 1>, dim3(grid_for(a.T)), dim3(kQkThreads), 0, stream,
-                         a, tab)
-            : launch_pdl(qk_norm_kernel<ROPE, 2>, dim3(grid_for((a.T + 1) / 2)), dim3(kQkThreads),
-                         0, stream, a, tab);
+            ? launch_pdl(qk_norm_kernel<ROPE, 1, KV>, dim3(grid_for(a.T)), dim3(kQkThreads), 0,
+                         stream, a, tab)
+            : launch_pdl(qk_norm_kernel<ROPE, 2, KV>, dim3(grid_for((a.T + 1) / 2)),
+                         dim3(kQkThreads), 0, stream, a, tab);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -371,12 +430,12 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
 
 cudaError_t launch_qk_norm_rope(const QkArgs &a, cudaStream_t stream)
 {
-    return launch_qk<true>(a, stream);
+    return a.cache_mode ? launch_qk<true, true>(a, stream) : launch_qk<true, false>(a, stream);
 }
 
 cudaError_t launch_qk_norm_ssmax(const QkArgs &a, cudaStream_t stream)
 {
-    return launch_qk<false>(a, stream);
+    return a.cache_mode ? launch_qk<false, true>(a, stream) : launch_qk<false, false>(a, stream);
 }
 
 uint64_t gate_head_magic(int32_t head_dim)

@@ -80,6 +80,40 @@ int check_qk(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride, const
     return BEAM_OK;
 }
 
+// The KV-cache arguments of the *_kv_fwd calls; on success fills the cache fields of `a`.
+int check_kv(beam::QkArgs &a, const void *v, int64_t v_row_stride, const int64_t *slot_mapping,
+             void *k_cache, void *v_cache, int64_t num_slots, int32_t cache_dtype, float k_scale,
+             float v_scale, int32_t n_kv)
+{
+    if (cache_dtype != 0 && cache_dtype != 1)
+        return BEAM_ERR_UNSUPPORTED;
+    if (num_slots < 0 || (cache_dtype == 1 && (!(k_scale > 0.0f) || !std::isfinite(k_scale) ||
+                                               !(v_scale > 0.0f) || !std::isfinite(v_scale))))
+        return BEAM_ERR_INVALID_ARG;
+    if (n_kv > 0 && (!v || !slot_mapping || !k_cache || !v_cache ||
+                     v_row_stride < (int64_t)n_kv * kHeadDim))
+        return BEAM_ERR_INVALID_ARG;
+    const uintptr_t cache_align = cache_dtype == 0 ? 16 : 8;
+    if (n_kv > 0 && (!aligned(v, 16) || v_row_stride % 8 != 0 || !aligned(slot_mapping, 8) ||
+                     !aligned(k_cache, cache_align) || !aligned(v_cache, cache_align)))
+        return BEAM_ERR_MISALIGNED;
+    a.v = v;
+    a.v_stride = v_row_stride;
+    a.slot = slot_mapping;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.num_slots = num_slots;
+    a.cache_mode = n_kv > 0 ? 1 + cache_dtype : 0;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    int ek, ev;
+    a.k_pow2 = std::frexp(k_scale, &ek) == 0.5f;
+    a.v_pow2 = std::frexp(v_scale, &ev) == 0.5f;
+    a.k_inv = a.k_pow2 ? std::ldexp(1.0f, 1 - ek) : 0.0f;
+    a.v_inv = a.v_pow2 ? std::ldexp(1.0f, 1 - ev) : 0.0f;
+    return BEAM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -297,6 +331,78 @@ int beam_qk_norm_ssmax_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_row
     if (T == 0)
         return BEAM_OK;
     beam::QkArgs a{};
+    a.q = q;
+    a.k = k;
+    a.q_stride = q_row_stride;
+    a.k_stride = k_row_stride;
+    a.wq = wq;
+    a.wk = wk;
+    a.pos = pos;
+    a.T = T;
+    a.n_q = n_q_heads;
+    a.n_kv = n_kv_heads;
+    a.eps = eps;
+    a.ssmax_base = ssmax_base;
+    a.ssmax_exp = ssmax_exp;
+    return cuda_status(beam::launch_qk_norm_ssmax(a, stream));
+}
+
+int beam_qk_norm_rope_kv_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride,
+                             const void *v, int64_t v_row_stride, const void *wq, const void *wk,
+                             const int64_t *pos, const int64_t *slot_mapping, void *k_cache,
+                             void *v_cache, int64_t num_slots, int32_t cache_dtype, float k_scale,
+                             float v_scale, int64_t T, int32_t n_q_heads, int32_t n_kv_heads,
+                             int32_t head_dim, float eps, float theta, cudaStream_t stream)
+{
+    int st = check_qk(q, k, q_row_stride, k_row_stride, wq, wk, pos, T, n_q_heads, n_kv_heads,
+                      head_dim, eps);
+    if (st != BEAM_OK)
+        return st;
+    if (!(theta > 0.0f) || !std::isfinite(theta))
+        return BEAM_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_OK;
+    beam::QkArgs a{};
+    st = check_kv(a, v, v_row_stride, slot_mapping, k_cache, v_cache, num_slots, cache_dtype,
+                  k_scale, v_scale, n_kv_heads);
+    if (st != BEAM_OK)
+        return st;
+    a.q = q;
+    a.k = k;
+    a.q_stride = q_row_stride;
+    a.k_stride = k_row_stride;
+    a.wq = wq;
+    a.wk = wk;
+    a.pos = pos;
+    a.T = T;
+    a.n_q = n_q_heads;
+    a.n_kv = n_kv_heads;
+    a.eps = eps;
+    a.inv_freq_host = rope_inv_freq(theta);
+    return cuda_status(beam::launch_qk_norm_rope(a, stream));
+}
+
+int beam_qk_norm_ssmax_kv_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride,
+                              const void *v, int64_t v_row_stride, const void *wq, const void *wk,
+                              const int64_t *pos, const int64_t *slot_mapping, void *k_cache,
+                              void *v_cache, int64_t num_slots, int32_t cache_dtype, float k_scale,
+                              float v_scale, int64_t T, int32_t n_q_heads, int32_t n_kv_heads,
+                              int32_t head_dim, float eps, float ssmax_base, float ssmax_exp,
+                              cudaStream_t stream)
+{
+    int st = check_qk(q, k, q_row_stride, k_row_stride, wq, wk, pos, T, n_q_heads, n_kv_heads,
+                      head_dim, eps);
+    if (st != BEAM_OK)
+        return st;
+    if (!(ssmax_base > 0.0f) || !std::isfinite(ssmax_base) || !std::isfinite(ssmax_exp))
+        return BEAM_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_OK;
+    beam::QkArgs a{};
+    st = check_kv(a, v, v_row_stride, slot_mapping, k_cache, v_cache, num_slots, cache_dtype,
+                  k_scale, v_scale, n_kv_heads);
+    if (st != BEAM_OK)
+        return st;
     a.q = q;
     a.k = k;
     a.q_stride = q_row_stride;

@@ -68,6 +68,11 @@ __device__ __forceinline__ void st_global(void *p, uint4 v)
                  : "memory");
 }
 
+__device__ __forceinline__ void st_global_v2(void *p, uint32_t a, uint32_t b)
+{
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+
 __device__ __forceinline__ uint32_t &word(uint4 &v, int i)
 {
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));

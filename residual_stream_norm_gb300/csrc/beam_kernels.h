@@ -64,6 +64,17 @@ struct QkArgs {
     // SSMax
     float ssmax_base;
     float ssmax_exp;
+    // KV-cache write (cache_mode 0: none, 1: BF16, 2: FP8 E4M3 of value / scale)
+    const void *v;          // [T, n_kv, 128] rows, v_stride elements apart
+    int64_t v_stride;
+    const int64_t *slot;    // [T] physical slot per token; < 0 or >= num_slots: not written
+    void *k_cache;          // [num_slots, n_kv, 128]
+    void *v_cache;
+    int64_t num_slots;
+    int32_t cache_mode;
+    float k_scale, v_scale;
+    float k_inv, v_inv;     // 1 / scale, used only where the scale is a power of two
+    bool k_pow2, v_pow2;
 };
 
 struct GateArgs {

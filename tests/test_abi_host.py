@@ -37,7 +37,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 12, names
+    assert len(names) == 14, names
     raw = ctypes.CDLL(rsn.LIB_PATH)
     for nm in names:
         assert hasattr(raw, nm), f"{nm} declared in the header but not exported"
@@ -112,6 +112,28 @@ def test_qk_parameter_checks(lib):
     assert qk(lib, fn="rope", extra=(float("nan"),)) == INVALID
     assert qk(lib, fn="ssmax", extra=(0.0, 0.1)) == INVALID
     assert qk(lib, fn="ssmax", extra=(2048.0, float("inf"))) == INVALID
+
+
+def qkv(lib, fn="rope", v=A, vs=8 * 128, slots=U, kc=A, vc=B, ns=64, dt=0, ksc=1.0, vsc=1.0,
+        T=4, nq=48, nk=8, D=128, extra=(10000.0,)):
+    f = lib.beam_qk_norm_rope_kv_fwd if fn == "rope" else lib.beam_qk_norm_ssmax_kv_fwd
+    return f(A, B, 48 * 128, 8 * 128, v, vs, A, B, U, slots, kc, vc, ns, dt, ksc, vsc, T, nq, nk,
+             D, 1e-6, *extra, None)
+
+
+@pytest.mark.parametrize("fn,extra", [("rope", (10000.0,)), ("ssmax", (2048.0, 0.1))])
+@pytest.mark.parametrize("kw,want", [
+    (dict(dt=2), UNSUPPORTED), (dict(dt=-1), UNSUPPORTED), (dict(ns=-1), INVALID),
+    (dict(v=None), INVALID), (dict(slots=None), INVALID), (dict(kc=None), INVALID),
+    (dict(vc=None), INVALID), (dict(vs=8 * 128 - 8), INVALID),
+    (dict(dt=1, ksc=0.0), INVALID), (dict(dt=1, vsc=float("inf")), INVALID),
+    (dict(dt=1, ksc=-2.0), INVALID), (dict(v=A + 8), MISALIGNED),
+    (dict(vs=8 * 128 + 4), MISALIGNED), (dict(slots=U + 4), MISALIGNED),
+    (dict(kc=A + 8), MISALIGNED), (dict(dt=1, vc=B + 4), MISALIGNED),
+    (dict(T=0, v=None, slots=None, kc=None, vc=None), OK),
+])
+def test_qk_kv_argument_checks(lib, fn, extra, kw, want):
+    assert qkv(lib, fn=fn, extra=extra, **kw) == want
 
 
 def gate(lib, out=A, attn=A, g=B, bias=U, T=4, nh=48, D=128, sa=6144, sg=6144, so=6144):
