@@ -71,6 +71,13 @@ def lib() -> ctypes.CDLL:
             so.orc_qk_norm_ssmax.argtypes = [u16p, u16p, i64, i64, u16p, u16p, i64p, i64, i32,
                                              i32, i32, f32, f32, f32, f32p]
             so.orc_attn_gate.argtypes = [u16p, u16p, u16p, f32p, i64, i32, i32, i64, i64, i64]
+            so.orc_sigmoid_f32.argtypes = [f32]
+            so.orc_sigmoid_f32.restype = f32
+            so.orc_exp_f32.argtypes = [f32]
+            so.orc_exp_f32.restype = f32
+            so.orc_grouped_topk.argtypes = [_P(ctypes.c_int32), f32p, f32p, f32p, i64, i32, i32,
+                                            i32, i32, f32p, _P(ctypes.c_int32)]
+            so.orc_grouped_topk.restype = None
             u8 = ctypes.c_uint8
             so.orc_fp8_e4m3_rne.argtypes = [f32]
             so.orc_fp8_e4m3_rne.restype = u8
@@ -221,6 +228,34 @@ def qk_norm_ssmax(q, k, wq, wk, pos, eps: float = 1e-6, base: float = 2048.0,
                             _ptr(pos, ctypes.c_int64), T, nq, nk, D, eps, base, expo,
                             _ptr(work, ctypes.c_float))
     return q, k
+
+
+def sigmoid_f32(z: float) -> float:
+    """FP32 sigmoid 1 / (1 + RN32(exp(-z))), FP32 add, IEEE division."""
+    return float(lib().orc_sigmoid_f32(float(z)))
+
+
+def exp_f32(x: float) -> float:
+    """exp(x) rounded once to FP32 (long double evaluation)."""
+    return float(lib().orc_exp_f32(float(x)))
+
+
+def grouped_topk(logits, bias, n_groups: int = 8, topk_groups: int = 4, top_k: int = 8):
+    """DeepSeek-V3-style grouped routing.  logits [T, E] float32, bias [E] float32.  Returns
+    (ids [T, top_k] int32, best first; weights [T, top_k] float32, renormalised, unscaled)."""
+    z = _f32(logits)
+    b = _f32(bias)
+    T, E = z.shape
+    assert b.shape == (E,) and E % n_groups == 0 and 1 <= topk_groups <= n_groups
+    ids = np.empty((T, top_k), dtype=np.int32)
+    w = np.empty((T, top_k), dtype=np.float32)
+    work = np.empty(2 * E + n_groups, dtype=np.float32)
+    iwork = np.empty(E + n_groups, dtype=np.int32)
+    lib().orc_grouped_topk(_ptr(ids, ctypes.c_int32), _ptr(w, ctypes.c_float),
+                           _ptr(z, ctypes.c_float), _ptr(b, ctypes.c_float), T, E, n_groups,
+                           topk_groups, top_k, _ptr(work, ctypes.c_float),
+                           _ptr(iwork, ctypes.c_int32))
+    return ids, w
 
 
 def fp8_e4m3_rne(x: float) -> int:

@@ -378,6 +378,94 @@ void orc_qk_norm_ssmax(uint16_t *q, uint16_t *k, int64_t q_stride, int64_t k_str
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* DeepSeek-V3-style grouped top-k routing (the step that produces the combine's inputs)        */
+/* ------------------------------------------------------------------------------------------ */
+
+/* FP32 sigmoid: 1 / (1 + e) with e = exp(-z) rounded once to FP32 (evaluated in long double),
+ * then an FP32 add and an IEEE FP32 division.  exp(-z) overflowing gives e = inf and 0. */
+float orc_sigmoid_f32(float z)
+{
+    float e = (float)expl(-(long double)z);
+    return 1.0f / (1.0f + e);
+}
+
+/* FP32 rounding of exp(x), evaluated in long double (test hook). */
+float orc_exp_f32(float x) { return (float)expl((long double)x); }
+
+/* Routing order: a number ranks above NaN; between numbers the larger value; ties (and NaN
+ * against NaN) go to the lower index. */
+static int ranks_above(float a, int32_t ia, float b, int32_t ib)
+{
+    int na = isnan(a), nb = isnan(b);
+    if (na != nb)
+        return nb;
+    if (!na && a != b)
+        return a > b;
+    return ia < ib;
+}
+
+/* Per token: s_e = sigmoid(logit_e); c_e = fp32(s_e + bias_e), the choice score.  Each of the
+ * G groups of E/G consecutive experts scores fp32(c_first + c_second), its two best choice
+ * scores; the topk_groups best groups stay eligible; the K best eligible experts by c are
+ * chosen, best first (ids[t, k]), and their weights are the renormalised sigmoid scores
+ * w_k = s_{ids_k} / S, S the FP32 sum of those scores in slot order, IEEE division.  The
+ * routed scaling (2.5) is applied later, by the combine.
+ * [vLLM] "MoE und Residual-Stream", bullet "MoE im DeepSeek-V3-Stil" (256 routed experts;
+ * sigmoid scores plus a correction bias choose the best 4 of 8 expert groups, then the top 8
+ * experts; the renormalised weights are scaled by 2.5) and bullet "FP32-Router"; [SGL]
+ * "稠密层与分组 MoE 路由" (grouped top-k from sigmoid scores and the correction bias, FP32
+ * coefficients).  The group score as the sum of the two best experts is DeepSeek-V3's rule,
+ * which the pages name without restating.  `work` holds 2E + G floats and E + G ints. */
+void orc_grouped_topk(int32_t *ids, float *w, const float *logits, const float *bias, int64_t T,
+                      int32_t E, int32_t G, int32_t topk_groups, int32_t K, float *work,
+                      int32_t *iwork)
+{
+    float *sc = work, *c = work + E, *gs = work + 2 * E;
+    int32_t *allowed = iwork, *gsel = iwork + E;
+    int32_t per = E / G;
+    for (int64_t t = 0; t < T; ++t) {
+        const float *z = logits + t * E;
+        for (int32_t e = 0; e < E; ++e) {
+            sc[e] = orc_sigmoid_f32(z[e]);
+            c[e] = sc[e] + bias[e];
+        }
+        for (int32_t g = 0; g < G; ++g) {
+            int32_t b1 = g * per;
+            for (int32_t e = g * per + 1; e < (g + 1) * per; ++e)
+                if (ranks_above(c[e], e, c[b1], b1))
+                    b1 = e;
+            int32_t b2 = -1;
+            for (int32_t e = g * per; e < (g + 1) * per; ++e)
+                if (e != b1 && (b2 < 0 || ranks_above(c[e], e, c[b2], b2)))
+                    b2 = e;
+            gs[g] = per > 1 ? c[b1] + c[b2] : c[b1];
+            gsel[g] = 0;
+        }
+        for (int32_t r = 0; r < topk_groups; ++r) {
+            int32_t best = -1;
+            for (int32_t g = 0; g < G; ++g)
+                if (!gsel[g] && (best < 0 || ranks_above(gs[g], g, gs[best], best)))
+                    best = g;
+            gsel[best] = 1;
+        }
+        for (int32_t e = 0; e < E; ++e)
+            allowed[e] = gsel[e / per];
+        float S = 0.0f;
+        for (int32_t k = 0; k < K; ++k) {
+            int32_t best = -1;
+            for (int32_t e = 0; e < E; ++e)
+                if (allowed[e] && (best < 0 || ranks_above(c[e], e, c[best], best)))
+                    best = e;
+            allowed[best] = 0;
+            ids[t * K + k] = best;
+            S = k == 0 ? sc[best] : S + sc[best];
+        }
+        for (int32_t k = 0; k < K; ++k)
+            w[t * K + k] = sc[ids[t * K + k]] / S;
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* KV-cache write (the step the Q/K kernel takes over)                                          */
 /* ------------------------------------------------------------------------------------------ */
 
@@ -446,8 +534,10 @@ void orc_kv_cache_write(void *k_cache, void *v_cache, const uint16_t *k, const u
                     ((uint16_t *)k_cache)[dst] = k[src_k];
                     ((uint16_t *)v_cache)[dst] = v[src_v];
                 } else {
-                    ((uint8_t *)k_cache)[dst] = orc_fp8_e4m3_rne(orc_bf16_to_f32(k[src_k]) / k_scale);
-                    ((uint8_t *)v_cache)[dst] = orc_fp8_e4m3_rne(orc_bf16_to_f32(v[src_v]) / v_scale);
+                    float kq = orc_bf16_to_f32(k[src_k]) / k_scale;
+                    float vq = orc_bf16_to_f32(v[src_v]) / v_scale;
+                    ((uint8_t *)k_cache)[dst] = orc_fp8_e4m3_rne(kq);
+                    ((uint8_t *)v_cache)[dst] = orc_fp8_e4m3_rne(vq);
                 }
             }
     }
