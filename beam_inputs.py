@@ -166,6 +166,20 @@ def kv_cache_case(T: int, n_kv: int = N_KV_HEADS, D: int = HEAD_DIM, slots_per_t
     return dict(v=v, slot_mapping=torch.from_numpy(slots), num_slots=num_slots)
 
 
+N_EXPERTS = 256
+N_GROUPS = 8
+TOPK_GROUPS = 4
+
+
+def routing_case(T: int, seed: int = 0, logit_std: float = 1.5, bias_std: float = 0.3) -> dict:
+    """FP32 router logits [T, 256] ~ N(0, logit_std^2) and an FP32 correction bias [256] ~
+    N(0, bias_std^2): the inputs of the grouped routing."""
+    g = rng(seed)
+    logits = torch.from_numpy(normal(g, (T, N_EXPERTS), std=logit_std))
+    bias = torch.from_numpy(normal(g, (N_EXPERTS,), std=bias_std))
+    return dict(logits=logits, bias=bias)
+
+
 def gate_case(T: int, n_heads: int = N_Q_HEADS, D: int = HEAD_DIM, seed: int = 0) -> dict:
     """attn ~ N(0, 1); gate ~ N(0, 2) read as variance 2 (std sqrt 2); per-head bias ~ N(0, 1)
     in FP32."""

@@ -55,6 +55,8 @@ KERNELS = list(BYTES_PER_TOKEN)
 # Rows beyond the five-kernel step, timed alone: the Q/K kernels fused with the KV-cache write
 # (V read, slot read, K' and V rows written as FP8 E4M3, 1 byte per element).
 KV_BYTES_PER_TOKEN = BYTES_PER_TOKEN["qk_norm_rope"] + NKV * D * 2 + 8 + 2 * NKV * D
+# Grouped routing: 256 FP32 logits read, 8 int32 ids and 8 FP32 weights written.
+ROUTE_BYTES_PER_TOKEN = bi.N_EXPERTS * 4 + K * 4 + K * 4
 SOURCES = {
     "qk_norm_rope": "attention.cu", "qk_norm_ssmax": "attention.cu", "attn_gate": "attention.cu",
     "boundary": "boundary.cu", "moe_combine_boundary": "boundary.cu",
@@ -379,9 +381,11 @@ def decode_chain_us(device, replays: int = 200) -> dict:
             "T": 1, "note": "working set fits in L2: time only, no HBM GB/s"}
 
 
-def kv_cache_rows(host: dict, device, peak: float, iters: int = 50) -> dict:
-    """The Q/K kernels fused with an FP8 KV-cache write at the step's T, each launch timed alone
-    with CUDA events (inputs larger than L2)."""
+def next_rows(host: dict, device, peak: float, iters: int = 50) -> dict:
+    """Rows beyond the five-kernel step at the step's T, each launch timed alone with CUDA
+    events: the Q/K kernels fused with an FP8 KV-cache write (inputs larger than L2), and the
+    grouped routing (16.8 MB of logits: L2-resident between launches, so its GB/s is not an
+    HBM figure; it is bound by its correctly rounded sigmoids)."""
     import residual_stream_norm_gb300 as rsn
     T = host["q_r"].shape[0]
     kv = bi.kv_cache_case(T=T, pad_frac=0.0, oob_frac=0.0, seed=7)
@@ -391,7 +395,12 @@ def kv_cache_rows(host: dict, device, peak: float, iters: int = 50) -> dict:
     slots = kv["slot_mapping"].to(device)
     kc = torch.zeros((kv["num_slots"], NKV, D), dtype=torch.uint8, device=device)
     vc = torch.zeros_like(kc)
+    rc = bi.routing_case(T=T, seed=8)
+    logits, rbias = rc["logits"].to(device), rc["bias"].to(device)
+    rids = torch.empty((T, K), dtype=torch.int32, device=device)
+    rw = torch.empty((T, K), dtype=torch.float32, device=device)
     runs = {
+        "grouped_topk": lambda: rsn.beam_grouped_topk_fwd(rids, rw, logits, rbias),
         "qk_norm_rope_kv_fp8": lambda: rsn.beam_qk_norm_rope_kv_fwd(
             d["q_r"], d["k_r"], v, d["wq_r"], d["wk_r"], d["pos_r"], slots, kc, vc,
             cache_dtype=rsn.CACHE_FP8_E4M3),
@@ -411,13 +420,18 @@ def kv_cache_rows(host: dict, device, peak: float, iters: int = 50) -> dict:
         e1.record()
         torch.cuda.synchronize(device)
         ms = e0.elapsed_time(e1) / iters
-        by = KV_BYTES_PER_TOKEN * T
+        by = (ROUTE_BYTES_PER_TOKEN if name == "grouped_topk" else KV_BYTES_PER_TOKEN) * T
         gbs = by / (ms * 1e-3) / 1e9
         out[name] = {"us": round(ms * 1e3, 2), "bytes_per_launch": by, "gb_s": round(gbs, 1),
                      "frac_of_peak": round(gbs / peak, 4),
                      "tokens_per_s": round(T / (ms * 1e-3), 1),
-                     "launches": iters, "cache": f"FP8 E4M3, {kv['num_slots']} slots, "
-                                                  "one distinct random slot per token"}
+                     "launches": iters}
+        if name != "grouped_topk":
+            out[name]["cache"] = (f"FP8 E4M3, {kv['num_slots']} slots, one distinct random "
+                                  "slot per token")
+        else:
+            out[name]["note"] = ("256 experts, 8 groups, top-4 groups, top-8; bound by the "
+                                 "correctly rounded FP32 sigmoids, not by HBM")
     return out
 
 
@@ -502,7 +516,7 @@ def run_gpu_arm(args) -> None:
            "path": "pinned host buffers -> cudaMemcpyAsync -> C ABI -> cudaMemcpyAsync -> host"}
 
     decode = decode_chain_us(device)
-    next_rows = kv_cache_rows(host, device, peak)
+    nxt = next_rows(host, device, peak)
 
     out = None
     if rank == 0:
@@ -525,7 +539,7 @@ def run_gpu_arm(args) -> None:
                        "l2": "inputs larger than L2 (every kernel streams >= 168 MB per launch; "
                              "L2 129 MB); no flush",
                        "parallelism": f"replicas x{ws}"},
-            "kernels": kernels, "roofline": roofline, "decode": decode, "next": next_rows,
+            "kernels": kernels, "roofline": roofline, "decode": decode, "next": nxt,
             "e2e": e2e,
             "cpu_baseline": cpu, "gpu_launches": gpu_launches * ws,
             "clocks": clocks.summary(t_wall0, t_wall1),

@@ -96,6 +96,12 @@ BEAM_API int beam_residual_operand(const float *x, float *b_out, int64_t count, 
  * rounding boundary.  Returns BEAM_ERR_INVALID_ARG for count < 0, count > 16384 or NULL arrays. */
 BEAM_API int beam_exact_square_sum(const float *v, int64_t count, float *out);
 
+/* Host-only helper: the FP32 sigmoid that beam_grouped_topk_fwd ranks experts by,
+ * sigma(z) = 1 / (1 + RN32(exp(-z))) (FP32 add, IEEE division, exp rounded once to FP32: FP32
+ * pair arithmetic with an FP64 pair fallback near rounding boundaries), for `count` values in
+ * host memory.  NaN stays NaN.  Returns BEAM_ERR_INVALID_ARG for count < 0 or NULL arrays. */
+BEAM_API int beam_routing_sigmoid(const float *z, float *out, int64_t count);
+
 /* Host-only helper: the FP32 cosine and sine that beam_qk_norm_rope_fwd uses for an FP32 rotary
  * angle, for `count` angles in host memory.  Each value is the FP32 rounding of the exact
  * cos / sin of the FP32 angle (except in rare near-tie cases), computed in FP32 pair arithmetic
@@ -244,6 +250,34 @@ BEAM_API int beam_qk_norm_ssmax_kv_fwd(void *q, void *k, int64_t q_row_stride, i
                               float v_scale, int64_t T, int32_t n_q_heads, int32_t n_kv_heads,
                               int32_t head_dim, float eps, float ssmax_base, float ssmax_exp,
                               cudaStream_t stream);
+
+/* DeepSeek-V3-style grouped top-k routing: the step that produces the MoE combine's inputs.
+ *
+ * [vLLM] "MoE und Residual-Stream", bullet "MoE im DeepSeek-V3-Stil" (256 routed experts,
+ * routed as in DeepSeek-V3: sigmoid scores plus a correction bias choose the best 4 of 8 expert
+ * groups, then the top 8 experts; the renormalised weights are scaled by 2.5) and bullet
+ * "FP32-Router" (logits in FP32); [SGL] "稠密层与分组 MoE 路由" (grouped top-k from the sigmoid
+ * scores and the expert correction bias; FP32 routing coefficients, the scaling applied in the
+ * combine).
+ *
+ * Per token t, with s_e = 1 / (1 + RN32(exp(-logit_e))) (as beam_routing_sigmoid) and the choice
+ * score c_e = fp32(s_e + bias_e):
+ *   - each of the 8 groups of 32 consecutive experts scores fp32(c_first + c_second), its two
+ *     best choice scores (DeepSeek-V3's group rule); the 4 best groups stay eligible;
+ *   - topk_ids[t, k], k < 8: the 8 best eligible experts by c, best first;
+ *   - topk_w[t, k] = s_{id_k} / S, S the FP32 sum of those 8 scores in slot order (IEEE
+ *     division): renormalised, not yet scaled -- beam_moe_combine_boundary_fwd applies the
+ *     routed scaling (2.5).
+ * Ranking: larger first; NaN below every number; ties to the lower index.  Because every
+ * sigmoid is the correctly rounded FP32 value, the choice is bit-reproducible.
+ *
+ *   logits [T, 256] fp32 (16-byte aligned rows), bias [256] fp32 (16-byte aligned)
+ *   topk_ids [T, 8] int32, topk_w [T, 8] fp32 (4-byte aligned)
+ * n_experts, n_groups, topk_groups, top_k must be 256, 8, 4, 8 (BEAM_ERR_UNSUPPORTED otherwise). */
+BEAM_API int beam_grouped_topk_fwd(int32_t *topk_ids, float *topk_w, const float *logits,
+                                   const float *bias, int64_t T, int32_t n_experts,
+                                   int32_t n_groups, int32_t topk_groups, int32_t top_k,
+                                   cudaStream_t stream);
 
 /* Sigmoid attention-output gate, before the output projection.
  *

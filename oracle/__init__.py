@@ -73,6 +73,8 @@ def lib() -> ctypes.CDLL:
             so.orc_attn_gate.argtypes = [u16p, u16p, u16p, f32p, i64, i32, i32, i64, i64, i64]
             so.orc_sigmoid_f32.argtypes = [f32]
             so.orc_sigmoid_f32.restype = f32
+            so.orc_sigmoid_array.argtypes = [f32p, f32p, i64]
+            so.orc_sigmoid_array.restype = None
             so.orc_exp_f32.argtypes = [f32]
             so.orc_exp_f32.restype = f32
             so.orc_grouped_topk.argtypes = [_P(ctypes.c_int32), f32p, f32p, f32p, i64, i32, i32,
@@ -233,6 +235,14 @@ def qk_norm_ssmax(q, k, wq, wk, pos, eps: float = 1e-6, base: float = 2048.0,
 def sigmoid_f32(z: float) -> float:
     """FP32 sigmoid 1 / (1 + RN32(exp(-z))), FP32 add, IEEE division."""
     return float(lib().orc_sigmoid_f32(float(z)))
+
+
+def sigmoid_array(z) -> np.ndarray:
+    """sigmoid_f32 over an array of float32 values."""
+    z = _f32(z)
+    out = np.empty_like(z)
+    lib().orc_sigmoid_array(_ptr(z, ctypes.c_float), _ptr(out, ctypes.c_float), z.size)
+    return out
 
 
 def exp_f32(x: float) -> float:

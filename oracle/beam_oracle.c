@@ -389,6 +389,12 @@ float orc_sigmoid_f32(float z)
     return 1.0f / (1.0f + e);
 }
 
+void orc_sigmoid_array(const float *z, float *out, int64_t count)
+{
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = orc_sigmoid_f32(z[i]);
+}
+
 /* FP32 rounding of exp(x), evaluated in long double (test hook). */
 float orc_exp_f32(float x) { return (float)expl((long double)x); }
 

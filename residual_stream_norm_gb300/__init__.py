@@ -20,10 +20,10 @@ from . import _build
 
 __all__ = ["BeamError", "build", "lib", "beam_abi_version", "beam_status_str",
            "beam_residual_scales", "beam_rope_cos_sin", "beam_residual_operand",
-           "beam_exact_square_sum", "beam_device_faults",
+           "beam_exact_square_sum", "beam_routing_sigmoid", "beam_device_faults",
            "beam_boundary_fwd", "beam_moe_combine_boundary_fwd",
            "beam_qk_norm_rope_fwd", "beam_qk_norm_ssmax_fwd", "beam_qk_norm_rope_kv_fwd",
-           "beam_qk_norm_ssmax_kv_fwd", "beam_attn_gate_fwd",
+           "beam_qk_norm_ssmax_kv_fwd", "beam_grouped_topk_fwd", "beam_attn_gate_fwd",
            "HEAD_DIM"]
 
 HEAD_DIM = 128
@@ -61,6 +61,7 @@ def lib() -> ctypes.CDLL:
             so.beam_rope_cos_sin.argtypes = [vp, vp, vp, i64]
             so.beam_residual_operand.argtypes = [vp, vp, i64, i32]
             so.beam_exact_square_sum.argtypes = [vp, i64, vp]
+            so.beam_routing_sigmoid.argtypes = [vp, vp, i64]
             so.beam_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
             so.beam_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, f32, vp, vp]
             so.beam_moe_combine_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, i64,
@@ -70,6 +71,7 @@ def lib() -> ctypes.CDLL:
             so.beam_qk_norm_ssmax_fwd.argtypes = [vp, vp, i64, i64, vp, vp, vp, i64, i32, i32,
                                                   i32, f32, f32, f32, vp]
             so.beam_attn_gate_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i64, i64, vp]
+            so.beam_grouped_topk_fwd.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, i32, vp]
             so.beam_qk_norm_rope_kv_fwd.argtypes = [vp, vp, i64, i64, vp, i64, vp, vp, vp, vp, vp,
                                                     vp, i64, i32, f32, f32, i64, i32, i32, i32,
                                                     f32, f32, vp]
@@ -77,11 +79,13 @@ def lib() -> ctypes.CDLL:
                                                      vp, vp, i64, i32, f32, f32, i64, i32, i32,
                                                      i32, f32, f32, f32, vp]
             for fn in ("beam_abi_version", "beam_residual_scales", "beam_rope_cos_sin",
-                       "beam_residual_operand", "beam_exact_square_sum", "beam_device_faults",
+                       "beam_residual_operand", "beam_exact_square_sum", "beam_routing_sigmoid",
+                       "beam_device_faults",
                        "beam_boundary_fwd",
                        "beam_moe_combine_boundary_fwd", "beam_qk_norm_rope_fwd",
                        "beam_qk_norm_ssmax_fwd", "beam_qk_norm_rope_kv_fwd",
-                       "beam_qk_norm_ssmax_kv_fwd", "beam_attn_gate_fwd"):
+                       "beam_qk_norm_ssmax_kv_fwd", "beam_grouped_topk_fwd",
+                       "beam_attn_gate_fwd"):
                 getattr(so, fn).restype = ctypes.c_int
             _lib = so
     return _lib
@@ -160,6 +164,17 @@ def beam_exact_square_sum(v) -> float:
     if st != 0:
         raise BeamError("beam_exact_square_sum", st)
     return out[0]
+
+
+def beam_routing_sigmoid(z):
+    """Host helper: the FP32 sigmoid the routing kernel ranks experts by (float32 in and out)."""
+    import numpy as np
+    a = np.ascontiguousarray(z, dtype=np.float32)
+    out = np.empty_like(a)
+    st = lib().beam_routing_sigmoid(a.ctypes.data, out.ctypes.data, a.size)
+    if st != 0:
+        raise BeamError("beam_routing_sigmoid", st)
+    return out
 
 
 def beam_residual_operand(x, n: int):
@@ -320,6 +335,29 @@ def beam_qk_norm_ssmax_kv_fwd(q, k, v, wq, wk, pos, slot_mapping, k_cache, v_cac
               _ptr(wk), _ptr(pos), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), num_slots,
               cache_dtype, k_scale, v_scale, T, nq, nk, HEAD_DIM, eps, ssmax_base, ssmax_exp,
               _stream(stream))
+
+
+def beam_grouped_topk_fwd(topk_ids, topk_w, logits, bias, n_groups: int = 8,
+                          topk_groups: int = 4, stream=None) -> None:
+    """DeepSeek-V3-style grouped routing: logits [T, 256] fp32, bias [256] fp32 -> topk_ids
+    [T, 8] int32 (best first) and topk_w [T, 8] fp32 (renormalised sigmoid scores)."""
+    def f32c(t, nm):
+        if not (isinstance(t, torch.Tensor) and t.dtype == torch.float32 and t.is_cuda and
+                t.is_contiguous()):
+            raise TypeError(f"{nm}: expected a contiguous CUDA float32 tensor")
+    f32c(logits, "logits")
+    f32c(bias, "bias")
+    f32c(topk_w, "topk_w")
+    if not (isinstance(topk_ids, torch.Tensor) and topk_ids.dtype == torch.int32 and
+            topk_ids.is_cuda and topk_ids.is_contiguous()):
+        raise TypeError("topk_ids: expected a contiguous CUDA int32 tensor")
+    T, E = logits.shape
+    k = topk_ids.shape[1] if topk_ids.dim() == 2 else -1
+    if bias.shape != (E,) or topk_ids.shape != (T, k) or topk_w.shape != (T, k):
+        raise ValueError("beam_grouped_topk_fwd: shape mismatch")
+    with torch.cuda.device(logits.device):
+        _call("beam_grouped_topk_fwd", _ptr(topk_ids), _ptr(topk_w), _ptr(logits), _ptr(bias), T,
+              E, n_groups, topk_groups, k, _stream(stream))
 
 
 def beam_attn_gate_fwd(out, attn, gate, bias, n_heads: int, head_dim: int = HEAD_DIM,

@@ -11,6 +11,7 @@
 #include "../../include/beam_boundary.h"
 #include "beam_kernels.h"
 #include "beam_exact.cuh"
+#include "beam_exp.cuh"
 #include "beam_f32x2.cuh"
 #include "beam_sincos.cuh"
 
@@ -202,6 +203,15 @@ int beam_exact_square_sum(const float *v, int64_t count, float *out)
         beam::exact_add(a, u, emax);
     }
     *out = beam::exact_round(a, emax);
+    return BEAM_OK;
+}
+
+int beam_routing_sigmoid(const float *z, float *out, int64_t count)
+{
+    if (count < 0 || (count > 0 && (!z || !out)))
+        return BEAM_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < count; ++i)
+        out[i] = beam::sigmoid_rounded(z[i]);
     return BEAM_OK;
 }
 
@@ -417,6 +427,30 @@ int beam_qk_norm_ssmax_kv_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_
     a.ssmax_base = ssmax_base;
     a.ssmax_exp = ssmax_exp;
     return cuda_status(beam::launch_qk_norm_ssmax(a, stream));
+}
+
+int beam_grouped_topk_fwd(int32_t *topk_ids, float *topk_w, const float *logits,
+                          const float *bias, int64_t T, int32_t n_experts, int32_t n_groups,
+                          int32_t topk_groups, int32_t top_k, cudaStream_t stream)
+{
+    if (n_experts != 256 || n_groups != 8 || topk_groups != 4 || top_k != 8)
+        return BEAM_ERR_UNSUPPORTED;
+    if (T < 0)
+        return BEAM_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_OK;
+    if (!topk_ids || !topk_w || !logits || !bias)
+        return BEAM_ERR_INVALID_ARG;
+    if (!aligned(logits, 16) || !aligned(bias, 16) || !aligned(topk_ids, 4) ||
+        !aligned(topk_w, 4))
+        return BEAM_ERR_MISALIGNED;
+    beam::RouteArgs a{};
+    a.logits = logits;
+    a.bias = bias;
+    a.ids = topk_ids;
+    a.weights = topk_w;
+    a.T = T;
+    return cuda_status(beam::launch_grouped_topk(a, stream));
 }
 
 int beam_attn_gate_fwd(void *out, const void *attn, const void *gate, const float *bias,

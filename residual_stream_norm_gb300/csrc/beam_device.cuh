@@ -68,6 +68,13 @@ __device__ __forceinline__ void st_global(void *p, uint4 v)
                  : "memory");
 }
 
+__device__ __forceinline__ float4 ld_stream_f4(const float *p)
+{
+    const uint4 v = ld_stream(p);
+    return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                       __uint_as_float(v.w));
+}
+
 __device__ __forceinline__ void st_global_v2(void *p, uint32_t a, uint32_t b)
 {
     asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(a), "r"(b) : "memory");

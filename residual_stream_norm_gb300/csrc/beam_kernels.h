@@ -77,6 +77,14 @@ struct QkArgs {
     bool k_pow2, v_pow2;
 };
 
+struct RouteArgs {
+    const float *logits;  // [T, 256] FP32 router logits
+    const float *bias;    // [256] FP32 correction bias
+    int32_t *ids;         // [T, 8] chosen experts, best first
+    float *weights;       // [T, 8] renormalised sigmoid scores
+    int64_t T;
+};
+
 struct GateArgs {
     void *out;
     const void *attn;
@@ -96,6 +104,7 @@ cudaError_t launch_moe_boundary(const BoundaryArgs &a, cudaStream_t stream);
 cudaError_t launch_qk_norm_rope(const QkArgs &a, cudaStream_t stream);
 cudaError_t launch_qk_norm_ssmax(const QkArgs &a, cudaStream_t stream);
 cudaError_t launch_attn_gate(const GateArgs &a, cudaStream_t stream);
+cudaError_t launch_grouped_topk(const RouteArgs &a, cudaStream_t stream);
 // ceil(2^32 / (head_dim / 8)): the multiplier that maps a gate vector index to its head.
 uint64_t gate_head_magic(int32_t head_dim);
 

@@ -37,7 +37,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 14, names
+    assert len(names) == 16, names
     raw = ctypes.CDLL(rsn.LIB_PATH)
     for nm in names:
         assert hasattr(raw, nm), f"{nm} declared in the header but not exported"
@@ -325,3 +325,39 @@ def test_exact_square_sum_rounds_ties_to_even_and_breaks_them_with_tiny_terms(li
 def test_exact_square_sum_argument_checks(lib):
     with pytest.raises(rsn.BeamError):
         rsn.beam_exact_square_sum(np.zeros(16385, np.float32))
+
+
+# ------------------------------------------------------------------------------------------
+# the routing sigmoid (host build of the kernels' arithmetic) and the routing call's checks
+# ------------------------------------------------------------------------------------------
+
+def test_routing_sigmoid_equals_the_oracle_on_a_sweep(lib):
+    # every 512th FP32 pattern over the range where the sigmoid is neither 0 nor 1 by overflow,
+    # plus random and edge values: bit-identical to the oracle's long-double evaluation
+    u = np.arange(0, 1 << 32, 512, dtype=np.uint64).astype(np.uint32)
+    z = u.view(np.float32)
+    z = z[np.isfinite(z) & (z > -89.5) & (z < 18.0)]
+    edges = np.array([0.0, -0.0, 16.9, 17.0, 17.1, -88.72, -88.7228, -88.73, -89.0, -100.0,
+                      100.0, 1e-30, -1e-30, np.inf, -np.inf], np.float32)
+    g = np.random.default_rng(9)
+    z = np.concatenate([z, edges, g.normal(0, 3, 200000).astype(np.float32)])
+    got = rsn.beam_routing_sigmoid(z)
+    want = oracle.sigmoid_array(z)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    assert np.isnan(rsn.beam_routing_sigmoid(np.array([np.nan], np.float32))).all()
+
+
+def route(lib, ids=A, w=B, logits=A + 4096, bias=B + 4096, T=4, E=256, G=8, TG=4, K=8):
+    return lib.beam_grouped_topk_fwd(ids, w, logits, bias, T, E, G, TG, K, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(E=128), UNSUPPORTED), (dict(G=4), UNSUPPORTED), (dict(TG=3), UNSUPPORTED),
+    (dict(K=6), UNSUPPORTED), (dict(T=-1), INVALID), (dict(ids=None), INVALID),
+    (dict(w=None), INVALID), (dict(logits=None), INVALID), (dict(bias=None), INVALID),
+    (dict(logits=A + 8), MISALIGNED), (dict(bias=B + 8), MISALIGNED),
+    (dict(ids=A + 2), MISALIGNED),
+    (dict(T=0, ids=None, w=None, logits=None, bias=None), OK),
+])
+def test_routing_argument_checks(lib, kw, want):
+    assert route(lib, **kw) == want
