@@ -416,12 +416,13 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
     RopeTable tab;
     for (int i = 0; i < kHalf; ++i)
         tab.inv_freq[i] = ROPE ? a.inv_freq_host[i] : 0.0f;
-    // Few tokens: one token per CTA spreads them over more SMs; otherwise two per CTA.
+    // Few tokens: one token per CTA spreads them over more SMs.  Otherwise four per CTA: the
+    // tile's 4 x 64 cos/sin pairs are then one per thread, and the per-tile barrier is rarer.
     const cudaError_t e =
-        a.T < 2 * 152
+        a.T < 4 * 152
             ? launch_pdl(qk_norm_kernel<ROPE, 1, KV>, dim3(grid_for(a.T)), dim3(kQkThreads), 0,
                          stream, a, tab)
-            : launch_pdl(qk_norm_kernel<ROPE, 2, KV>, dim3(grid_for((a.T + 1) / 2)),
+            : launch_pdl(qk_norm_kernel<ROPE, 4, KV>, dim3(grid_for((a.T + 3) / 4)),
                          dim3(kQkThreads), 0, stream, a, tab);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
