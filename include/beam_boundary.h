@@ -287,7 +287,9 @@ BEAM_API int beam_grouped_topk_fwd(int32_t *topk_ids, float *topk_w, const float
  * fused in one kernel).
  *
  * out[t, h*D + d] = bf16( attn * (1 / (1 + expf(-z))) ),  z = fp32(gate[t, h*D + d] + bias[h]),
- * with CUDA's full-accuracy expf, FP32 add and IEEE division.
+ * with CUDA's full-accuracy expf, an FP32 add and the hardware reciprocal (within one FP32 ulp;
+ * exact for 1/2 and 1/inf).  The output scales with the sigmoid, so these few FP32 ulps move it
+ * by at most one BF16 ulp.
  *
  *   out, attn, gate  [T, n_heads*head_dim] bf16 rows at the given strides (elements, >= the row
  *   length, multiples of 8); out may be the same buffer as attn (same stride) for in-place use.

@@ -359,9 +359,20 @@ __device__ __forceinline__ int gate_head(int v, uint64_t m)
     return (int)(((uint64_t)(uint32_t)v * m) >> 32);
 }
 
+// Hardware reciprocal (rcp.approx.f32, subnormals kept): within one FP32 ulp.
+__device__ __forceinline__ float rcp_approx(float x)
+{
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // out = bf16(attn * 1/(1 + expf(-(gate + bias_h)))).  One CTA per row, 4 vectors per thread
 // per pass, all loads of a pass issued before any arithmetic; the additions, the reciprocal's
-// operand and the product run on packed pairs, expf and the IEEE reciprocal per element.
+// operand and the product run on packed pairs, expf and the reciprocal per element.  The output
+// is a product of attn and the sigmoid (nothing cancels), so the few FP32 ulps of expf and of
+// the hardware reciprocal move it by at most one BF16 ulp; 1/(1 + 1) = 0.5 and 1/inf = 0 stay
+// exact, so a zero gate input halves attn exactly and a -inf bias switches a head off.
 __global__ void __launch_bounds__(256) attn_gate_kernel(const GateArgs a)
 {
     const int vpr = (a.n_heads * a.head_dim) >> 3;
@@ -395,7 +406,7 @@ __global__ void __launch_bounds__(256) attn_gate_kernel(const GateArgs a)
                         const f2 z = add2(widen(word(gv[i], j)), b);
                         const f2 e = make_f2(expf(-lo_of(z)), expf(-hi_of(z)));
                         const f2 den = add2(one, e);
-                        const f2 sig = make_f2(__frcp_rn(lo_of(den)), __frcp_rn(hi_of(den)));
+                        const f2 sig = make_f2(rcp_approx(lo_of(den)), rcp_approx(hi_of(den)));
                         word(o, j) = narrow(mul2(widen(word(av[i], j)), sig));
                     }
                     st_global(out + 16 * (int64_t)v, o);
