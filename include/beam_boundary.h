@@ -77,6 +77,13 @@ BEAM_API int beam_residual_scales(int32_t n, float *alpha, float *s);
  * No counterpart on the pages: a diagnostic of this library. */
 BEAM_API int beam_device_faults(uint32_t *flags, int clear);
 
+/* Diagnostic: exercises the copy-timeout path of the persistent kernels without a fault.  One
+ * CTA arms an mbarrier for 16 bytes that no copy delivers, waits with the kernels' bounded wait
+ * for limit_ns nanoseconds (1 us .. 2 s), gives up and sets bit 0 of the device fault word, as a
+ * ring kernel whose copies stalled would; nothing is left in flight.  Asynchronous on `stream`;
+ * read the result with beam_device_faults().  BEAM_ERR_INVALID_ARG for a limit out of range. */
+BEAM_API int beam_selftest_copy_timeout(int64_t limit_ns, cudaStream_t stream);
+
 /* Host-only helper: the residual operand b = bf16(x / s), s = fp32(sqrt(n)), returned as FP32
  * values, for `count` BF16 values x given as FP32 (low 16 bits zero) in host memory, exactly as
  * the boundary kernels form it ("Tiefenskalierte Residuen").  The kernels take b = bf16(RN(x y))

@@ -21,6 +21,7 @@ from . import _build
 __all__ = ["BeamError", "build", "lib", "beam_abi_version", "beam_status_str",
            "beam_residual_scales", "beam_rope_cos_sin", "beam_residual_operand",
            "beam_exact_square_sum", "beam_routing_sigmoid", "beam_device_faults",
+           "beam_selftest_copy_timeout",
            "beam_boundary_fwd", "beam_moe_combine_boundary_fwd",
            "beam_qk_norm_rope_fwd", "beam_qk_norm_ssmax_fwd", "beam_qk_norm_rope_kv_fwd",
            "beam_qk_norm_ssmax_kv_fwd", "beam_grouped_topk_fwd", "beam_attn_gate_fwd",
@@ -63,6 +64,7 @@ def lib() -> ctypes.CDLL:
             so.beam_exact_square_sum.argtypes = [vp, i64, vp]
             so.beam_routing_sigmoid.argtypes = [vp, vp, i64]
             so.beam_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+            so.beam_selftest_copy_timeout.argtypes = [i64, vp]
             so.beam_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, f32, vp, vp]
             so.beam_moe_combine_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, i64,
                                                          i32, i32, i32, f32, vp, vp]
@@ -80,7 +82,7 @@ def lib() -> ctypes.CDLL:
                                                      i32, f32, f32, f32, vp]
             for fn in ("beam_abi_version", "beam_residual_scales", "beam_rope_cos_sin",
                        "beam_residual_operand", "beam_exact_square_sum", "beam_routing_sigmoid",
-                       "beam_device_faults",
+                       "beam_device_faults", "beam_selftest_copy_timeout",
                        "beam_boundary_fwd",
                        "beam_moe_combine_boundary_fwd", "beam_qk_norm_rope_fwd",
                        "beam_qk_norm_ssmax_fwd", "beam_qk_norm_rope_kv_fwd",
@@ -164,6 +166,12 @@ def beam_exact_square_sum(v) -> float:
     if st != 0:
         raise BeamError("beam_exact_square_sum", st)
     return out[0]
+
+
+def beam_selftest_copy_timeout(limit_ns: int = 20_000_000, stream=None) -> None:
+    """Diagnostic: run the kernels' copy-timeout path once (a wait nothing completes gives up
+    after limit_ns and sets bit 0 of the device fault word)."""
+    _call("beam_selftest_copy_timeout", limit_ns, _stream(stream))
 
 
 def beam_routing_sigmoid(z):

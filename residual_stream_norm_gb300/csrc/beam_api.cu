@@ -152,6 +152,13 @@ int beam_device_faults(uint32_t *flags, int clear)
     return cuda_status(e);
 }
 
+int beam_selftest_copy_timeout(int64_t limit_ns, cudaStream_t stream)
+{
+    if (limit_ns < 1000 || limit_ns > 2000000000)
+        return BEAM_ERR_INVALID_ARG;
+    return cuda_status(beam::launch_copy_timeout_selftest((unsigned long long)limit_ns, stream));
+}
+
 int beam_residual_operand(const float *x, float *b_out, int64_t count, int32_t n)
 {
     if (n < 1 || count < 0 || (count > 0 && (!x || !b_out)))

@@ -108,6 +108,10 @@ cudaError_t launch_grouped_topk(const RouteArgs &a, cudaStream_t stream);
 // ceil(2^32 / (head_dim / 8)): the multiplier that maps a gate vector index to its head.
 uint64_t gate_head_magic(int32_t head_dim);
 
+// Runs the copy-timeout path once: a wait that nothing completes gives up after limit_ns and
+// raises bit 0 of the fault word.
+cudaError_t launch_copy_timeout_selftest(unsigned long long limit_ns, cudaStream_t stream);
+
 // The device fault word of the current device (bit 0: a kernel gave up waiting for its own bulk
 // copies); synchronous.
 cudaError_t read_fault_word(unsigned int *value, bool clear);

@@ -83,10 +83,11 @@ __device__ __forceinline__ unsigned long long global_ns()
 }
 
 // Wait for phase `parity` of `bar`, giving up when the CTA's shared `fail` flag is set (some
-// thread already gave up) or after kWaitLimitNs (then this thread sets `fail`).  False when it
+// thread already gave up) or after `limit_ns` (then this thread sets `fail`).  False when it
 // gave up.
 __device__ __forceinline__ bool mbar_wait_or_fail(uint64_t *bar, uint32_t parity,
-                                                  volatile int *fail)
+                                                  volatile int *fail,
+                                                  unsigned long long limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
@@ -94,7 +95,7 @@ __device__ __forceinline__ bool mbar_wait_or_fail(uint64_t *bar, uint32_t parity
     while (!mbar_try_wait(bar, parity)) {
         if (*fail)
             return false;
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() - t0 > limit_ns) {
             *fail = 1;
             return false;
         }

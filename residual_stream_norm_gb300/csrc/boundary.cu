@@ -680,6 +680,39 @@ cudaError_t launch_moe_boundary(const BoundaryArgs &a, cudaStream_t stream)
     return launch<true>(a, stream);
 }
 
+namespace {
+
+// The copy-timeout path on its own: one CTA arms an mbarrier for 16 bytes of transactions that
+// no copy ever delivers, waits for it with the ring kernels' bounded wait (limit `limit_ns`),
+// gives up, and raises the fault bit exactly as a ring kernel would.  Nothing is in flight when
+// it returns.
+__global__ void copy_timeout_selftest_kernel(unsigned long long limit_ns)
+{
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int fail;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fail = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        mbar_arrive_expect_tx(&bar, 16u);  // the arrival comes; the 16 bytes never do
+    __syncthreads();
+    const bool ok = mbar_wait_or_fail(&bar, 0u, &fail, limit_ns);
+    __syncthreads();
+    if (threadIdx.x == 0 && (!ok || fail))
+        atomicOr(&g_fault_word, kFaultCopyTimeout);
+}
+
+}  // namespace
+
+cudaError_t launch_copy_timeout_selftest(unsigned long long limit_ns, cudaStream_t stream)
+{
+    copy_timeout_selftest_kernel<<<1, 64, 0, stream>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t read_fault_word(unsigned int *value, bool clear)
 {
     cudaError_t e = cudaMemcpyFromSymbol(value, g_fault_word, sizeof(unsigned int));

@@ -37,7 +37,7 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 16, names
+    assert len(names) == 17, names
     raw = ctypes.CDLL(rsn.LIB_PATH)
     for nm in names:
         assert hasattr(raw, nm), f"{nm} declared in the header but not exported"
@@ -361,3 +361,8 @@ def route(lib, ids=A, w=B, logits=A + 4096, bias=B + 4096, T=4, E=256, G=8, TG=4
 ])
 def test_routing_argument_checks(lib, kw, want):
     assert route(lib, **kw) == want
+
+
+def test_selftest_copy_timeout_limit_checks(lib):
+    assert lib.beam_selftest_copy_timeout(10, None) == INVALID
+    assert lib.beam_selftest_copy_timeout(3_000_000_000, None) == INVALID

@@ -5,6 +5,8 @@ The boundary chain of "Serving Reflection Beam auf vLLM ab Tag 0" ("MoE und Resi
 ("三明治归一化与深度缩放残差").  Bar: every BF16 output within 1 ulp of the oracle and at least
 99.9 % bit-identical; the FP32 per-token scales within 2e-6 relative.
 """
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -234,3 +236,21 @@ def test_near_tie_row_sums_round_exactly(T):
     want = oracle.boundary(h, xb, u16(c["w_post"]), u16(c["w_pre"]), 3)
     assert np.array_equal(got[2][:, 0], want[2][:, 0]), "r must be the exactly rounded value"
     check(got, want, f"near-tie rows T={T}")
+
+
+def test_copy_timeout_path_sets_the_fault_word_and_leaves_the_context_usable():
+    # A wait that nothing completes (an mbarrier armed for bytes no copy delivers) must give up
+    # after its limit, raise the fault bit and return; the context then runs the next kernel.
+    torch.cuda.synchronize()
+    assert rsn.beam_device_faults(clear=True) == 0
+    t0 = time.perf_counter()
+    rsn.beam_selftest_copy_timeout(20_000_000)  # 20 ms
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    assert rsn.beam_device_faults(clear=True) == 1
+    assert 0.015 < waited < 5.0
+    c = bi.boundary_case(T=4, n=5, seed=0)
+    got = run_gpu(c["h"], c["x"], c["w_post"], c["w_pre"], 5)
+    want = oracle.boundary(u16(c["h"]), u16(c["x"]), u16(c["w_post"]), u16(c["w_pre"]), 5)
+    check(got, want, "after the timeout")
+    assert rsn.beam_device_faults() == 0
