@@ -10,7 +10,8 @@
 // "Sandwich-Norm" and "Tiefenskalierte Residuen"; [SGL] "三明治归一化与深度缩放残差").  The MoE
 // variant first forms the top-K weighted expert sum ([vLLM] change 3; [SGL] "稠密层与分组 MoE
 // 路由").  Nothing between the stages goes back to HBM: per row the kernel reads x (or the K
-// expert rows) and h once and writes h' and y once; the norm weights come from L1/L2.
+// expert rows) and h once and writes h' and y once; the norm weights come from L1/L2 (rows
+// kernel) or are parked once per CTA in shared memory (ring kernel).
 //
 // Two layouts, same arithmetic (boundary_chain):
 //  * rows kernel (few tokens, e.g. batch-1 decode): one CTA per token row; each thread owns VPT
@@ -444,8 +445,8 @@ __global__ void __launch_bounds__(kRingConsumers + 32, MOE ? 3 : 4)
     const int tid = threadIdx.x;
     const int KIN = MOE ? a.K : 1;
     const uint32_t stage_bytes = (uint32_t)(KIN + 1) * kSlice;
-    // the plain boundary's consumer threads park their slices of w_post and w_pre here
-    // ([2][VPT][NC] vectors); the MoE variant, whose stages are large, reads them through L1
+    // the consumer threads park their slices of w_post and w_pre here ([2][VPT][NC] vectors):
+    // read from shared memory inside the chain, they cost no long-latency loads
     uint4 *wsm = reinterpret_cast<uint4 *>(ring + (size_t)stages * stage_bytes);
     const int64_t first = blockIdx.x;
     const int64_t stride = gridDim.x;
@@ -508,12 +509,10 @@ __global__ void __launch_bounds__(kRingConsumers + 32, MOE ? 3 : 4)
     }
 
     // ---- consumer warps ----------------------------------------------------------------------
-    if constexpr (!MOE) {
 #pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            wsm[i * NC + tid] = weight_vec(a.w_post, tid + i * NC, nvec);
-            wsm[(VPT + i) * NC + tid] = weight_vec(a.w_pre, tid + i * NC, nvec);
-        }
+    for (int i = 0; i < VPT; ++i) {
+        wsm[i * NC + tid] = weight_vec(a.w_post, tid + i * NC, nvec);
+        wsm[(VPT + i) * NC + tid] = weight_vec(a.w_pre, tid + i * NC, nvec);
     }
     pdl_wait();
     const int lane = tid & 31;
@@ -557,16 +556,9 @@ __global__ void __launch_bounds__(kRingConsumers + 32, MOE ? 3 : 4)
                 parity ^= 1u;
             }
         }
-        if constexpr (MOE)
-            boundary_chain<VPT>(
-                a, row, xv, hv, [&](int k) { return weight_vec(a.w_post, tid + k * NC, nvec); },
-                [&](int k) { return weight_vec(a.w_pre, tid + k * NC, nvec); }, red, xred, pred, NC,
-                true, [] {});
-        else
-            boundary_chain<VPT>(
-                a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
-                [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, true,
-                [] {});
+        boundary_chain<VPT>(
+            a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
+            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, true, [] {});
     }
     if (tid == 0 && fail)
         atomicOr(&g_fault_word, kFaultCopyTimeout);
@@ -635,11 +627,12 @@ cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
     const int chunks = (nvec + kRingConsumers - 1) / kRingConsumers;
     if (a.T >= 4 * (int64_t)sms && chunks <= 8) {
         const size_t stage = (size_t)((MOE ? a.K : 1) + 1) * kRingConsumers * 16;
-        const size_t weights = MOE ? 0 : (size_t)2 * chunks * kRingConsumers * 16;
-        // stages: about 32 KB per CTA for the plain boundary (4 CTAs per SM), 3 for the MoE
-        // variant (whose stages hold K + 1 slices); at most 16
-        int stages = MOE ? 3 : (int)((32 * 1024) / stage);
-        stages = stages < 3 ? 3 : (stages > kRingMaxStages ? kRingMaxStages : stages);
+        const size_t weights = (size_t)2 * chunks * kRingConsumers * 16;
+        // stages: about 32 KB per CTA for the plain boundary (4 CTAs per SM); 2 for the MoE
+        // variant, whose stages hold K + 1 slices, so that its weights fit beside them at 3 CTAs
+        // per SM; at most 16
+        int stages = MOE ? 2 : (int)((32 * 1024) / stage);
+        stages = stages < 2 ? 2 : (stages > kRingMaxStages ? kRingMaxStages : stages);
         const size_t smem = kRingHeader + stages * stage + weights;
         switch (chunks) {
         case 1: return launch_ring<1, MOE>(a, stages, smem, sms, stream);
