@@ -336,6 +336,28 @@ def time_oracle(host: dict, tokens: int, threads: int, i: int = 0) -> float:
 # arms
 # ---------------------------------------------------------------------------------------------
 
+def copy_ceiling(device, nbytes: int = 1 << 30, reps: int = 20) -> dict:
+    """A device-to-device copy of `nbytes` (well above L2) timed in this run: the bandwidth a
+    plain stream of reads and writes reaches on this GPU right now, as a second ceiling beside
+    the committed measured peak."""
+    src = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    dst = torch.empty_like(src)
+    src.fill_(1)
+    for _ in range(3):
+        dst.copy_(src)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e0.record()
+    for _ in range(reps):
+        dst.copy_(src)
+    e1.record()
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / reps
+    del src, dst
+    return {"gb_s": round(2 * nbytes / (ms * 1e-3) / 1e9, 1), "bytes_moved": 2 * nbytes,
+            "how": "torch copy_ of a 1 GiB device buffer (read + write), 20 reps, CUDA events"}
+
+
 def decode_chain_us(device, replays: int = 200) -> dict:
     """Batch-1 decode: 104 boundary launches n = 1..104 captured in one CUDA graph."""
     import residual_stream_norm_gb300 as rsn
@@ -543,6 +565,11 @@ def run_gpu_arm(args) -> None:
 
     decode = decode_chain_us(device)
     nxt = next_rows(host, device, peak)
+    ceiling = copy_ceiling(device)
+    roofline["copy_ceiling_gbs"] = ceiling["gb_s"]
+    roofline["frac_of_copy_ceiling"] = round(roofline["achieved"] / ceiling["gb_s"], 4)
+    for v in kernels.values():
+        v["frac_of_copy_ceiling"] = round(v["gb_s"] / ceiling["gb_s"], 4)
 
     out = None
     if rank == 0:
@@ -565,7 +592,8 @@ def run_gpu_arm(args) -> None:
                        "l2": "inputs larger than L2 (every kernel streams >= 168 MB per launch; "
                              "L2 129 MB); no flush",
                        "parallelism": f"replicas x{ws}"},
-            "kernels": kernels, "roofline": roofline, "decode": decode, "next": nxt,
+            "kernels": kernels, "roofline": roofline, "copy_ceiling": ceiling,
+            "decode": decode, "next": nxt,
             "e2e": e2e,
             "cpu_baseline": cpu, "gpu_launches": gpu_launches * ws,
             "clocks": clocks.summary(t_wall0, t_wall1),

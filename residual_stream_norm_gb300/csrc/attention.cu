@@ -11,11 +11,12 @@
 //  * Sigmoid output gate: [vLLM] "Attention", bullet "Sigmoid-Output-Gate"; [SGL]
 //    "混合注意力与输出门控" and the kernel-fusion paragraph (bias add, sigmoid, multiply fused).
 //
-// Q/K layout: a CTA of 256 threads takes tiles of TT tokens; each quad of lanes owns one
-// (token, head) item of 128 elements, two items per quad per pass, all loads of a pass issued
-// before any arithmetic (see qk_norm_kernel).  The per-token factors (64 cos/sin pairs, or the
-// SSMax scale) are computed once per token into shared memory while the first loads are in
-// flight.  cos/sin are the FP32 roundings of the exact values of the FP32 angle
+// Q/K layout: each quad of lanes owns one (token, head) item of 128 elements.  Without a KV cache
+// a CTA of 256 threads takes tiles of 4 tokens, two items per quad per pass, all loads of a pass
+// issued before any arithmetic (qk_norm_kernel); with a cache, a persistent kernel prefetches
+// 2-token tiles into shared memory with bulk copies a tile ahead (qk_ring_kernel).  The
+// per-token factors (64 cos/sin pairs, or the SSMax scale) are computed once per token into
+// shared memory.  cos/sin are the FP32 roundings of the exact values of the FP32 angle
 // (beam_sincos.cuh), so the rotation matches the oracle bit for bit even where its two products
 // nearly cancel.  Element arithmetic runs on packed FP32 pairs (beam_f32x2.cuh).
 
@@ -26,6 +27,7 @@
 #include "beam_f32x2.cuh"
 #include "beam_kernels.h"
 #include "beam_sincos.cuh"
+#include "beam_tma.cuh"
 
 namespace beam {
 namespace {
@@ -38,6 +40,7 @@ constexpr int kIPP = 2;                 // heads per quad per pass, loads issued
 
 struct RopeTable {
     float inv_freq[kHalf];  // fp32(theta^(-2i/128)), formed on the host in double
+    float neg_zero;         // -0.0f, a launch parameter so that the compiler cannot see its value
 };
 
 // The rare exact path: this quad's head sum of the FP32 squares in 128-bit fixed point, rounded
@@ -112,16 +115,198 @@ __device__ __forceinline__ void cache_store(void *cache, int64_t e, uint4 o, int
     st_global_v2((char *)cache + e, w[0] | (w[1] << 16), w[2] | (w[3] << 16));
 }
 
-// Work items are the (token, head) pairs of a tile of TT tokens.  A quad of lanes owns one head:
-// lane q holds the 16-byte vectors q, q+4, q+8 and q+12 of its 128 elements, so a warp load
-// reads 64 contiguous bytes per head, and the rotation partners (element i < 64 and i + 64,
-// i.e. vectors q and q+8, q+4 and q+12) sit in the same lane.  The head's sum of squares needs a
-// two-step butterfly over the quad.  The per-token factors of the tile (64 cos/sin pairs, or
-// the SSMax scale) are computed once into shared memory while the first loads are in flight;
-// the Q and K norm weights are held in shared memory as FP32.  With a KV cache the items also
-// include the V heads: their rows go to the V cache as they are, and the K rows go to the K
-// cache as they are stored (after the norm and rotation), in the same pass.  Quads of one warp
-// may then take different paths, so every shuffle is masked to its quad.
+// A quad of lanes owns one (token, head) item of 128 elements: lane q holds the 16-byte vectors
+// q + 4 k (k = 0..3) of the head, so the rotation partners (element i < 64 and i + 64, i.e.
+// vectors q + 4 k and q + 4 (k + 2)) sit in the same lane, and the head's sum of squares needs a
+// two-step butterfly over the quad.  Register jj of the lane holds vector q + 4 (jj ^ sw): the
+// persistent kernel flips the order on odd quads (sw = 1) so that a warp's shared-memory reads
+// spread over all banks; the direct kernel uses sw = 0.  With a KV cache the items also include
+// the V heads: their rows go to the V cache as they are, and the K rows go to the K cache as they
+// are stored (after the norm and rotation).  Quads of one warp may then take different paths, so
+// every shuffle is masked to its quad.
+
+// The per-token factors of one tile: 64 cos/sin pairs per token (RoPE), or the SSMax query
+// scale.  cos/sin are the FP32 roundings of the exact values of the FP32 angle.
+template <bool ROPE, int TT>
+__device__ __forceinline__ void tile_factors(const QkArgs &a, const RopeTable &tab, int64_t t0,
+                                             int nt, float (&cs)[TT][kHalf],
+                                             float (&sn)[TT][kHalf], float (&scale_q)[TT])
+{
+    const int tid = threadIdx.x;
+    if constexpr (ROPE) {
+        for (int i = tid; i < nt * kHalf; i += blockDim.x) {
+            const int tt = i / kHalf, f = i - tt * kHalf;
+            const float p = (float)a.pos[t0 + tt];
+            const float ang = __fmul_rn(p, tab.inv_freq[f]);
+            float sv, cv;
+            if (fabsf(ang) < kSinCosMaxArg)
+                sincos_rounded(ang, &sv, &cv);  // FP32 rounding of exact cos / sin
+            else
+                sincosf(ang, &sv, &cv);
+            cs[tt][f] = cv;
+            sn[tt][f] = sv;
+        }
+    } else {
+        if (tid < nt) {
+            const float p1 = (float)(a.pos[t0 + tid] + 1);
+            const float b = __fadd_rn(1.0f, __fdiv_rn(p1, a.ssmax_base));
+            scale_q[tid] = powf(b, a.ssmax_exp);
+        }
+    }
+}
+
+// One item: normalise, rotate / scale, round, store (and write the KV cache).  `v` holds the
+// lane's four vectors (see above), `row` the item's row in global memory (nullptr: an inactive
+// item, whose lanes still take part in every shuffle), `tt` / `hd` its token within the tile and
+// its head (Q heads, then K, then V), `cst` / `snt` / `sq` the token's factors.  All lanes of the
+// warp call it together.
+template <bool ROPE, bool KV>
+__device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], char *row, int tt,
+                                        int hd, int64_t t0, int q, int sw, unsigned qmask,
+                                        const float (&wsm)[2][kHeadDim], const float *cst,
+                                        const float *snt, float sq, f2 nz)
+{
+    const int nqk = a.n_q + a.n_kv;
+    const bool act = row != nullptr;  // uniform across each quad
+    const bool isq = hd < a.n_q;
+    // the cache slot of a K or V item (-1: no cache, padding or out of range)
+    int64_t cslot = -1;
+    if (KV && act && !isq) {
+        const int64_t s = a.slot[t0 + tt];
+        cslot = s >= 0 && s < a.num_slots ? s : -1;
+    }
+    if (KV && hd >= nqk) {  // a V item: into the V cache, unchanged
+        if (cslot >= 0) {
+            const int64_t e0 = (cslot * a.n_kv + (hd - nqk)) * kHeadDim;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+                cache_store(a.v_cache, e0 + 8 * (q + 4 * (jj ^ sw)), v[jj], a.cache_mode,
+                            a.v_scale, a.v_inv, a.v_pow2);
+        }
+        return;
+    }
+    f2 x[4][4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp)
+            x[jj][pp] = widen(word(v[jj], pp));
+    float ms;
+    if constexpr (ROPE) {
+        // The rotation can cancel, so an FP32 ulp of r could move an output by more than a BF16
+        // ulp: the head sum is rounded as the exact sum would be.
+        Sum2x2 acc = {0ull, 0ull};
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp)
+                sum2_add(acc, mul2(x[jj][pp], x[jj][pp]));
+        Sum2 tot = sum_merge(Sum2{lo_of(acc.hi), lo_of(acc.lo)}, Sum2{hi_of(acc.hi), hi_of(acc.lo)});
+#pragma unroll
+        for (int off = 1; off < 4; off <<= 1) {
+            Sum2 o;
+            o.hi = __shfl_xor_sync(qmask, tot.hi, off);
+            o.lo = __shfl_xor_sync(qmask, tot.lo, off);
+            tot = sum_merge(tot, o);
+        }
+        ms = sum_value(tot);
+        const bool tie = near_tie(tot.hi, tot.lo, ms);  // the same in the quad
+        if constexpr (KV) {
+            if (tie)  // rare
+                ms = head_sum_exact(row, q, qmask);
+        } else if (__any_sync(0xffffffffu, tie)) {
+            // rare; the whole warp joins the (warp-wide) shuffles
+            const float exact = head_sum_exact(row, q, qmask);
+            if (tie)
+                ms = exact;
+        }
+    } else {
+        // The outputs only scale with r: a plain FP32 sum in a fixed order (per lane, then the
+        // quad butterfly) moves them by at most one BF16 ulp.
+        f2 s0 = 0ull, s1 = 0ull;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                if (pp & 1)
+                    s1 = fma2(x[jj][pp], x[jj][pp], s1);
+                else
+                    s0 = fma2(x[jj][pp], x[jj][pp], s0);
+            }
+        const f2 s2 = add2(s0, s1);
+        ms = __fadd_rn(lo_of(s2), hi_of(s2));
+        ms = __fadd_rn(ms, __shfl_xor_sync(qmask, ms, 1));
+        ms = __fadd_rn(ms, __shfl_xor_sync(qmask, ms, 2));
+    }
+    const f2 rr = splat(rms_inv_pow2(ms, 1.0f / kHeadDim, a.eps));
+    const float *wrow = wsm[isq ? 0 : 1];
+    f2 qh[4][4];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+        const int e0 = 8 * (q + 4 * (jj ^ sw));
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+            const f2 w = *reinterpret_cast<const f2 *>(&wrow[e0 + 2 * pp]);
+            qh[jj][pp] = mul2(mul2(x[jj][pp], rr), w);
+        }
+    }
+    f2 out[4][4];
+    if constexpr (ROPE) {
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+            const int i0 = 8 * (q + 4 * (jj ^ sw));  // first-half element index (< 64)
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp) {
+                const f2 c = *reinterpret_cast<const f2 *>(&cst[i0 + 2 * pp]);
+                const f2 sv = *reinterpret_cast<const f2 *>(&snt[i0 + 2 * pp]);
+                const f2 lo = qh[jj][pp], hi = qh[jj + 2][pp];  // (jj + 2) ^ sw = (jj ^ sw) + 2
+                // out_i = q_i c - q_{i+64} s;  out_{i+64} = q_{i+64} c + q_i s, each product
+                // rounded.  A packed product that feeds a packed add is fused into one FMA by the
+                // compiler, so each product is formed as fma(x, y, nz) with nz = -0 (the same
+                // value as the rounded product, signed zeros included), which it cannot fuse.
+                out[jj][pp] = sub2(fma2(lo, c, nz), fma2(hi, sv, nz));
+                out[jj + 2][pp] = add2(fma2(hi, c, nz), fma2(lo, sv, nz));
+            }
+        }
+    } else {
+        const f2 sc = splat(isq ? sq : 1.0f);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp)
+                out[jj][pp] = isq ? mul2(qh[jj][pp], sc) : qh[jj][pp];
+    }
+    if (act) {
+        const int64_t e0 = KV && cslot >= 0 ? (cslot * a.n_kv + (hd - a.n_q)) * kHeadDim : 0;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            uint4 o;
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp)
+                word(o, pp) = narrow(out[jj][pp]);
+            const int vi = q + 4 * (jj ^ sw);
+            st_global(row + 16 * vi, o);
+            if (KV && cslot >= 0)  // a K item: the stored K' also into the K cache
+                cache_store(a.k_cache, e0 + 8 * vi, o, a.cache_mode, a.k_scale, a.k_inv,
+                            a.k_pow2);
+        }
+    }
+}
+
+// Global row of item (token t, head hd): Q heads, then K, then V.
+__device__ __forceinline__ char *item_row(const QkArgs &a, int64_t t, int hd, int nqk)
+{
+    if (hd < a.n_q)
+        return (char *)a.q + 2 * (t * a.q_stride + (int64_t)hd * kHeadDim);
+    if (hd < nqk)
+        return (char *)a.k + 2 * (t * a.k_stride + (int64_t)(hd - a.n_q) * kHeadDim);
+    return (char *)a.v + 2 * (t * a.v_stride + (int64_t)(hd - nqk) * kHeadDim);  // only read
+}
+
+// Direct kernel (few tokens): a CTA of 256 threads takes tiles of TT tokens, each quad two items
+// per pass, all loads of a pass issued (straight from global memory) before any arithmetic; the
+// tile's factors are computed while the first loads are in flight.  The Q and K norm weights are
+// held in shared memory as FP32.
 template <bool ROPE, int TT, bool KV>
 __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, const RopeTable tab)
 {
@@ -163,7 +348,6 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
 #pragma unroll
             for (int m = 0; m < kIPP; ++m) {
                 const int j = base + slot + kSlots * m;
-                row[m] = nullptr;
                 int tt = 0, hd = j < nitems ? j : 0;  // inactive items map to (0, 0)
                 while (hd >= nheads) {  // at most TT - 1 steps
                     hd -= nheads;
@@ -171,183 +355,152 @@ __global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, 
                 }
                 tok[m] = tt;
                 head[m] = hd;
+                row[m] = j < nitems ? item_row(a, t0 + tt, hd, nqk) : nullptr;
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
-                    v[m][jj] = zero;
-                if (j < nitems) {
-                    const int64_t t = t0 + tt;
-                    if (hd < a.n_q)
-                        row[m] = (char *)a.q + 2 * (t * a.q_stride + (int64_t)hd * kHeadDim);
-                    else if (hd < nqk)
-                        row[m] = (char *)a.k +
-                                 2 * (t * a.k_stride + (int64_t)(hd - a.n_q) * kHeadDim);
-                    else  // V rows are only read
-                        row[m] = (char *)a.v +
-                                 2 * (t * a.v_stride + (int64_t)(hd - nqk) * kHeadDim);
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-                        v[m][jj] = ld_plain(row[m] + 16 * (q + 4 * jj));
-                }
+                    v[m][jj] = row[m] ? ld_plain(row[m] + 16 * (q + 4 * jj)) : zero;
             }
             // ---- per-token factors of the tile, once, while the first loads fly -------------
             if (base == 0) {
-                if constexpr (ROPE) {
-                    for (int i = tid; i < nt * kHalf; i += kQkThreads) {
-                        const int tt = i / kHalf, f = i - tt * kHalf;
-                        const float p = (float)a.pos[t0 + tt];
-                        const float ang = __fmul_rn(p, tab.inv_freq[f]);
-                        float sv, cv;
-                        if (fabsf(ang) < kSinCosMaxArg)
-                            sincos_rounded(ang, &sv, &cv);  // FP32 rounding of exact cos / sin
-                        else
-                            sincosf(ang, &sv, &cv);
-                        cs[buf][tt][f] = cv;
-                        sn[buf][tt][f] = sv;
-                    }
-                } else {
-                    if (tid < nt) {
-                        const float p1 = (float)(a.pos[t0 + tid] + 1);
-                        const float b = __fadd_rn(1.0f, __fdiv_rn(p1, a.ssmax_base));
-                        scale_q[buf][tid] = powf(b, a.ssmax_exp);
-                    }
-                }
+                tile_factors<ROPE, TT>(a, tab, t0, nt, cs[buf], sn[buf], scale_q[buf]);
                 __syncthreads();
             }
-            // ---- normalise, rotate / scale, round, store -----------------------------------
 #pragma unroll
-            for (int m = 0; m < kIPP; ++m) {
-                const bool act = row[m] != nullptr;  // uniform across each quad
-                const int tt = tok[m];
-                const bool isq = head[m] < a.n_q;
-                // the cache slot of a K or V item (-1: no cache, padding or out of range)
-                int64_t cslot = -1;
-                if (KV && act && !isq) {
-                    const int64_t s = a.slot[t0 + tt];
-                    cslot = s >= 0 && s < a.num_slots ? s : -1;
-                }
-                if (KV && head[m] >= nqk) {  // a V item: into the V cache, unchanged
-                    if (cslot >= 0) {
-                        const int64_t e0 = (cslot * a.n_kv + (head[m] - nqk)) * kHeadDim;
-#pragma unroll
-                        for (int jj = 0; jj < 4; ++jj)
-                            cache_store(a.v_cache, e0 + 8 * (q + 4 * jj), v[m][jj], a.cache_mode,
-                                        a.v_scale, a.v_inv, a.v_pow2);
-                    }
-                    continue;
-                }
-                f2 x[4][4];
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                    for (int pp = 0; pp < 4; ++pp)
-                        x[jj][pp] = widen(word(v[m][jj], pp));
-                float ms;
-                if constexpr (ROPE) {
-                    // The rotation can cancel, so an FP32 ulp of r could move an output by more
-                    // than a BF16 ulp: the head sum is rounded as the exact sum would be.
-                    Sum2x2 acc = {0ull, 0ull};
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                        for (int pp = 0; pp < 4; ++pp)
-                            sum2_add(acc, mul2(x[jj][pp], x[jj][pp]));
-                    Sum2 tot = sum_merge(Sum2{lo_of(acc.hi), lo_of(acc.lo)},
-                                         Sum2{hi_of(acc.hi), hi_of(acc.lo)});
-#pragma unroll
-                    for (int off = 1; off < 4; off <<= 1) {
-                        Sum2 o;
-                        o.hi = __shfl_xor_sync(qmask, tot.hi, off);
-                        o.lo = __shfl_xor_sync(qmask, tot.lo, off);
-                        tot = sum_merge(tot, o);
-                    }
-                    ms = sum_value(tot);
-                    const bool tie = near_tie(tot.hi, tot.lo, ms);  // the same in the quad
-                    if constexpr (KV) {
-                        if (tie)  // rare
-                            ms = head_sum_exact(row[m], q, qmask);
-                    } else if (__any_sync(0xffffffffu, tie)) {
-                        // rare; the whole warp joins the (warp-wide) shuffles
-                        const float exact = head_sum_exact(row[m], q, qmask);
-                        if (tie)
-                            ms = exact;
-                    }
-                } else {
-                    // The outputs only scale with r: a plain FP32 sum in a fixed order (per lane,
-                    // then the quad butterfly) moves them by at most one BF16 ulp.
-                    f2 s0 = 0ull, s1 = 0ull;
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                        for (int pp = 0; pp < 4; ++pp) {
-                            if (pp & 1)
-                                s1 = fma2(x[jj][pp], x[jj][pp], s1);
-                            else
-                                s0 = fma2(x[jj][pp], x[jj][pp], s0);
-                        }
-                    const f2 s2 = add2(s0, s1);
-                    ms = __fadd_rn(lo_of(s2), hi_of(s2));
-                    ms = __fadd_rn(ms, __shfl_xor_sync(qmask, ms, 1));
-                    ms = __fadd_rn(ms, __shfl_xor_sync(qmask, ms, 2));
-                }
-                const f2 rr = splat(rms_inv(ms, (float)kHeadDim, a.eps));
-                const float *wrow = wsm[isq ? 0 : 1];
-                f2 qh[4][4];
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int e0 = 8 * (q + 4 * jj);
-#pragma unroll
-                    for (int pp = 0; pp < 4; ++pp) {
-                        const f2 w = *reinterpret_cast<const f2 *>(&wrow[e0 + 2 * pp]);
-                        qh[jj][pp] = mul2(mul2(x[jj][pp], rr), w);
-                    }
-                }
-                f2 out[4][4];
-                if constexpr (ROPE) {
-#pragma unroll
-                    for (int jj = 0; jj < 2; ++jj) {
-                        const int i0 = 8 * (q + 4 * jj);  // first-half element index (< 64)
-#pragma unroll
-                        for (int pp = 0; pp < 4; ++pp) {
-                            const f2 c = *reinterpret_cast<const f2 *>(&cs[buf][tt][i0 + 2 * pp]);
-                            const f2 sv = *reinterpret_cast<const f2 *>(&sn[buf][tt][i0 + 2 * pp]);
-                            const f2 lo = qh[jj][pp], hi = qh[jj + 2][pp];
-                            // out_i = q_i c - q_{i+64} s;  out_{i+64} = q_{i+64} c + q_i s.
-                            // Scalar IEEE intrinsics: a packed product feeding a packed add is
-                            // fused into one FMA by the compiler, which would skip the rounding
-                            // of the products.
-                            out[jj][pp] = make_f2(
-                                __fsub_rn(__fmul_rn(lo_of(lo), lo_of(c)), __fmul_rn(lo_of(hi), lo_of(sv))),
-                                __fsub_rn(__fmul_rn(hi_of(lo), hi_of(c)), __fmul_rn(hi_of(hi), hi_of(sv))));
-                            out[jj + 2][pp] = make_f2(
-                                __fadd_rn(__fmul_rn(lo_of(hi), lo_of(c)), __fmul_rn(lo_of(lo), lo_of(sv))),
-                                __fadd_rn(__fmul_rn(hi_of(hi), hi_of(c)), __fmul_rn(hi_of(lo), hi_of(sv))));
-                        }
-                    }
-                } else {
-                    const f2 sc = splat(isq ? scale_q[buf][tt] : 1.0f);
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj)
-#pragma unroll
-                        for (int pp = 0; pp < 4; ++pp)
-                            out[jj][pp] = isq ? mul2(qh[jj][pp], sc) : qh[jj][pp];
-                }
-                if (act) {
-                    const int64_t e0 =
-                        KV && cslot >= 0 ? (cslot * a.n_kv + (head[m] - a.n_q)) * kHeadDim : 0;
-#pragma unroll
-                    for (int jj = 0; jj < 4; ++jj) {
-                        uint4 o;
-#pragma unroll
-                        for (int pp = 0; pp < 4; ++pp)
-                            word(o, pp) = narrow(out[jj][pp]);
-                        st_global(row[m] + 16 * (q + 4 * jj), o);
-                        if (KV && cslot >= 0)  // a K item: the stored K' also into the K cache
-                            cache_store(a.k_cache, e0 + 8 * (q + 4 * jj), o, a.cache_mode,
-                                        a.k_scale, a.k_inv, a.k_pow2);
-                    }
-                }
-            }
+            for (int m = 0; m < kIPP; ++m)
+                qk_item<ROPE, KV>(a, v[m], row[m], tok[m], head[m], t0, q, 0, qmask, wsm,
+                                  cs[buf][tok[m]], sn[buf][tok[m]],
+                                  ROPE ? 0.0f : scale_q[buf][tok[m]], splat(tab.neg_zero));
         }
+    }
+}
+
+// Persistent kernel (many tokens): CTAs loop over tiles of kRingTT tokens.  One thread issues
+// bulk copies (TMA) of a tile's Q, K (and V) rows into one of two shared-memory buffers a tile
+// ahead, so the next tile's reads are in flight while the warps work on this one; the factors of
+// the next tile are computed at the same point.  A tile's items are then read from shared memory,
+// quad by quad, and finished as in the direct kernel.  The block has one quad per two items of a
+// tile (at most 256 threads), so every quad has the same work between the per-tile barriers:
+// 224 threads for 2 x 56 heads, 256 with the V heads.  Every
+// wait on a copy is bounded (beam_tma.cuh); a CTA that gives up raises the fault word.
+constexpr int kRingTT = 2;
+
+template <bool ROPE, bool KV>
+__device__ __forceinline__ void issue_tile(const QkArgs &a, int64_t tile, int nheads,
+                                           unsigned char *dst, uint64_t *bar)
+{
+    const int64_t t0 = tile * kRingTT;
+    const int nt = (int)(a.T - t0 < kRingTT ? a.T - t0 : kRingTT);
+    const int nqk = a.n_q + a.n_kv;
+    mbar_arrive_expect_tx(bar, (uint32_t)(nt * nheads) * 256u);
+    for (int tt = 0; tt < nt; ++tt) {
+        const int64_t t = t0 + tt;
+        unsigned char *d = dst + (size_t)tt * nheads * 256;
+        if (a.n_q > 0)
+            bulk_g2s(d, (const char *)a.q + 2 * t * a.q_stride, (uint32_t)a.n_q * 256u, bar);
+        if (a.n_kv > 0) {
+            bulk_g2s(d + (size_t)a.n_q * 256, (const char *)a.k + 2 * t * a.k_stride,
+                     (uint32_t)a.n_kv * 256u, bar);
+            if (KV)
+                bulk_g2s(d + (size_t)nqk * 256, (const char *)a.v + 2 * t * a.v_stride,
+                         (uint32_t)a.n_kv * 256u, bar);
+        }
+    }
+}
+
+template <bool ROPE, bool KV>
+__global__ void __launch_bounds__(kQkThreads, 3)
+    qk_ring_kernel(const QkArgs a, const RopeTable tab)
+{
+    constexpr int TT = kRingTT;
+    extern __shared__ __align__(128) unsigned char qbuf[];  // [2][TT * nheads * 256 bytes]
+    __shared__ __align__(8) uint64_t full[2];
+    __shared__ __align__(16) float cs[2][TT][kHalf];
+    __shared__ __align__(16) float sn[2][TT][kHalf];
+    __shared__ float scale_q[2][TT];
+    __shared__ __align__(16) float wsm[2][kHeadDim];
+    __shared__ int fail;
+    const int nqk = a.n_q + a.n_kv;
+    const int nheads = nqk + (KV ? a.n_kv : 0);
+    const size_t tile_bytes = (size_t)TT * nheads * 256;
+    const unsigned qmask = KV ? 0xfu << (threadIdx.x & 28) : 0xffffffffu;
+    const int tid = threadIdx.x;
+    const int q = tid & 3;
+    const int slot = tid >> 2;
+    const int nslots = blockDim.x >> 2;  // quads: the launch sizes the block to the tile
+    const int sw = slot & 1;
+    pdl_launch_dependents();
+    for (int i = tid; i < 2 * kHeadDim; i += blockDim.x) {
+        const int which = i >> 7, e = i & 127;
+        const bool have = which == 0 ? a.n_q > 0 : a.n_kv > 0;
+        const uint16_t *w = (const uint16_t *)(which == 0 ? a.wq : a.wk);
+        wsm[which][e] = have ? __uint_as_float((uint32_t)w[e] << 16) : 0.0f;
+    }
+    if (tid == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        fail = 0;
+        fence_mbar_init();
+    }
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    const int64_t ntiles = (a.T + TT - 1) / TT;
+    const int64_t first = blockIdx.x, stride = gridDim.x;
+    __syncthreads();
+    pdl_wait();
+    uint32_t uses[2] = {0u, 0u};  // copies issued into each buffer (thread 0)
+    if (first < ntiles) {
+        if (tid == 0) {
+            issue_tile<ROPE, KV>(a, first, nheads, qbuf, &full[0]);
+            uses[0] = 1;
+        }
+        const int64_t t0 = first * TT;
+        tile_factors<ROPE, TT>(a, tab, t0, (int)(a.T - t0 < TT ? a.T - t0 : TT), cs[0], sn[0],
+                               scale_q[0]);
+    }
+    int k = 0;
+    for (int64_t tile = first; tile < ntiles; tile += stride, ++k) {
+        const int b = k & 1;
+        __syncthreads();  // tile k - 1 is done: its buffer and factors may be refilled
+        const int64_t next = tile + stride;
+        if (next < ntiles) {
+            if (tid == 0) {
+                issue_tile<ROPE, KV>(a, next, nheads, qbuf + (b ^ 1) * tile_bytes, &full[b ^ 1]);
+                ++uses[b ^ 1];
+            }
+            const int64_t tn = next * TT;
+            tile_factors<ROPE, TT>(a, tab, tn, (int)(a.T - tn < TT ? a.T - tn : TT), cs[b ^ 1],
+                                   sn[b ^ 1], scale_q[b ^ 1]);
+        }
+        (void)mbar_wait_or_fail(&full[b], (uint32_t)(k >> 1) & 1u, &fail);
+        const int64_t t0 = tile * TT;
+        const int nt = (int)(a.T - t0 < TT ? a.T - t0 : TT);
+        const int nitems = nt * nheads;
+        const unsigned char *tb = qbuf + b * tile_bytes;
+        // items j = slot, slot + nslots, ...: read from shared memory one at a time (short
+        // latency); every warp runs the same number of rounds
+        for (int j = slot; j < ((nitems + nslots - 1) / nslots) * nslots; j += nslots) {
+            int tt = 0, hd = j < nitems ? j : 0;  // inactive items map to (0, 0)
+            while (hd >= nheads) {  // at most TT - 1 steps
+                hd -= nheads;
+                ++tt;
+            }
+            char *row = j < nitems ? item_row(a, t0 + tt, hd, nqk) : nullptr;
+            const unsigned char *src = tb + (size_t)(row ? j : 0) * 256;
+            uint4 v[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+                v[jj] = row ? *reinterpret_cast<const uint4 *>(src + 16 * (q + 4 * (jj ^ sw)))
+                            : zero;
+            qk_item<ROPE, KV>(a, v, row, tt, hd, t0, q, sw, qmask, wsm, cs[b][tt], sn[b][tt],
+                              ROPE ? 0.0f : scale_q[b][tt], splat(tab.neg_zero));
+        }
+    }
+    // Every copy issued was waited for above unless a wait gave up; then make sure none is still
+    // landing before the CTA leaves (bounded), and raise the fault word.
+    if (tid == 0 && fail) {
+        for (int bb = 0; bb < 2; ++bb)
+            if (uses[bb] > 0)
+                (void)mbar_wait(&full[bb], (uses[bb] - 1u) & 1u);
+        atomicOr(a.fault_word, kFaultCopyTimeout);
     }
 }
 
@@ -421,20 +574,69 @@ inline unsigned grid_for(int64_t units)
     return (unsigned)(units < (int64_t)(1 << 30) ? units : (int64_t)(1 << 30));
 }
 
+// Largest double buffer of the persistent Q/K kernel: 64 KB keeps 3 CTAs on an SM (2 tiles of
+// 2 tokens x 64 heads x 256 bytes for Beam's 48 + 8 heads with a KV cache).
+constexpr size_t kQkRingMaxSmem = 64 * 1024;
+
+// The persistent kernel with a KV cache: one quad per two items of a tile (256 threads for
+// 2 x 64 heads), as many CTAs as the double buffer lets the SMs hold.
+template <bool ROPE>
+cudaError_t launch_ring_qk(const QkArgs &a, const RopeTable &tab, int sms, int nheads,
+                           size_t smem, cudaStream_t stream)
+{
+    auto kern = qk_ring_kernel<ROPE, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    const int items = kRingTT * nheads;
+    int threads = 4 * ((items + 1) / 2);
+    threads = threads > kQkThreads ? kQkThreads : (threads + 31) / 32 * 32;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    if (e != cudaSuccess)
+        return e;
+    if (per_sm < 1)
+        return cudaErrorInvalidConfiguration;
+    const int64_t ntiles = (a.T + kRingTT - 1) / kRingTT;
+    const int64_t slots = (int64_t)sms * per_sm;
+    return launch_pdl(kern, dim3((unsigned)(ntiles < slots ? ntiles : slots)), dim3(threads),
+                      smem, stream, a, tab);
+}
+
 template <bool ROPE, bool KV>
-cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
+cudaError_t launch_qk(const QkArgs &a_in, cudaStream_t stream)
 {
     RopeTable tab;
     for (int i = 0; i < kHalf; ++i)
-        tab.inv_freq[i] = ROPE ? a.inv_freq_host[i] : 0.0f;
-    // Few tokens: one token per CTA spreads them over more SMs.  Otherwise four per CTA: the
-    // tile's 4 x 64 cos/sin pairs are then one per thread, and the per-tile barrier is rarer.
-    const cudaError_t e =
-        a.T < 4 * 152
-            ? launch_pdl(qk_norm_kernel<ROPE, 1, KV>, dim3(grid_for(a.T)), dim3(kQkThreads), 0,
-                         stream, a, tab)
-            : launch_pdl(qk_norm_kernel<ROPE, 4, KV>, dim3(grid_for((a.T + 3) / 4)),
-                         dim3(kQkThreads), 0, stream, a, tab);
+        tab.inv_freq[i] = ROPE ? a_in.inv_freq_host[i] : 0.0f;
+    tab.neg_zero = -0.0f;
+    QkArgs a = a_in;
+    a.fault_word = fault_word_device();
+    if (!a.fault_word)
+        return cudaErrorInvalidSymbol;
+    const int sms = device_sm_count();
+    const bool many = a.T >= 4 * (int64_t)sms;
+    cudaError_t e;
+    if constexpr (KV) {
+        // Many tokens with a KV cache: the persistent kernel, one tile ahead (it keeps the V
+        // rows' reads and the cache writes in flight beside the Q/K work).
+        const int nheads = a.n_q + 2 * a.n_kv;
+        const size_t smem = (size_t)2 * kRingTT * nheads * 256;
+        if (many && smem <= kQkRingMaxSmem) {
+            e = launch_ring_qk<ROPE>(a, tab, sms, nheads, smem, stream);
+            return e != cudaSuccess ? e : cudaGetLastError();
+        }
+    }
+    // Without the cache the direct kernel is the faster one: its 4-token tiles keep two heads'
+    // loads in flight per quad and need no barrier per tile.  Few tokens: one token per CTA
+    // spreads them over more SMs.
+    if (many)
+        e = launch_pdl(qk_norm_kernel<ROPE, 4, KV>, dim3(grid_for((a.T + 3) / 4)),
+                       dim3(kQkThreads), 0, stream, a, tab);
+    else
+        e = launch_pdl(qk_norm_kernel<ROPE, 1, KV>, dim3(grid_for(a.T)), dim3(kQkThreads), 0,
+                       stream, a, tab);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -192,10 +192,18 @@ __device__ __forceinline__ void pdl_wait()
     asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-// r = 1 / sqrt(ms / len + eps) with IEEE division and square root.
+// r = 1 / sqrt(ms / len + eps) with IEEE division and square root.  The reciprocal is the
+// correctly rounded __frcp_rn: the same value as the division 1 / x.
 __device__ __forceinline__ float rms_inv(float ms, float len, float eps)
 {
-    return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ms, len), eps)));
+    return __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(ms, len), eps)));
+}
+
+// The same for a power-of-two length with inv_len = 1 / len (exact): ms / len and ms * inv_len
+// are the correct roundings of the same real number, so they are equal.
+__device__ __forceinline__ float rms_inv_pow2(float ms, float inv_len, float eps)
+{
+    return __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ms, inv_len), eps)));
 }
 
 }  // namespace beam

@@ -8,8 +8,10 @@
 // Caution: the compiler fuses a packed product that feeds a packed add/sub into one packed FMA
 // (the product is then not rounded), despite the .rn modifiers and even through an opaque move.
 // Packed products therefore only feed packed adds where the product is exact (squares of BF16
-// values); an inexact product followed by an add uses the scalar __fmul_rn / __fadd_rn
-// intrinsics, which are never fused.
+// values).  An inexact product followed by an add is formed either with the scalar __fmul_rn /
+// __fadd_rn intrinsics, which are never fused, or as a packed fma(x, y, nz) whose addend nz is
+// -0 held in a launch parameter: the rounded product exactly (a zero product keeps its sign),
+// and an FMA followed by an add is not fused.
 #pragma once
 
 #include <cmath>

@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
 
 // ---- ring kernel: persistent, warp-specialised TMA pipeline ---------------------------------
 //
-// A CTA has NC consumer threads (kRingConsumers, 4 warps) and one producer warp.  Its rows are
+// A CTA has NC consumer threads (a multiple of 32) and one producer warp.  Its rows are
 // blockIdx.x, blockIdx.x + gridDim.x, ...; each row is cut into VPT chunks of NC 16-byte
 // vectors, and consumer thread t owns vector c * NC + t of chunk c.  A unit of work is one chunk
 // of one row; its stage holds KIN input slices (the x chunk, or the K expert chunks) and the h
@@ -422,12 +422,18 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
 // bulk copies have landed (transaction bytes), `empty` when all consumer warps have read the
 // stage (one arrive per warp).  The producer keeps `stages` units in flight.
 
-constexpr int kRingConsumers = 128;
 constexpr int kRingHeader = 256;  // 2 x up to 16 mbarriers
 constexpr int kRingMaxStages = 16;
 
-template <int VPT, bool MOE>
-__global__ void __launch_bounds__(kRingConsumers + 32, MOE ? 3 : 4)
+// Ring shapes: consumer threads per CTA and CTAs per SM.  The MoE variant's stages hold K + 1
+// slices, so it keeps slices small (4 consumer warps) at 3 CTAs per SM.
+constexpr int kMoeConsumers = 128;
+constexpr int kMoeCtasPerSm = 3;
+constexpr int kPlainConsumers = 128;
+constexpr int kPlainCtasPerSm = 3;
+
+template <int NC, int VPT, bool MOE, int MINB>
+__global__ void __launch_bounds__(NC + 32, MINB)
     boundary_ring_kernel(const BoundaryArgs a, int stages)
 {
     extern __shared__ __align__(128) unsigned char dyn[];
@@ -439,7 +445,6 @@ __global__ void __launch_bounds__(kRingConsumers + 32, MOE ? 3 : 4)
     __shared__ float pred[32];
     __shared__ int fail;
 
-    constexpr int NC = kRingConsumers;
     constexpr uint32_t kSlice = NC * 16;
     const int nvec = a.H >> 3;
     const int tid = threadIdx.x;
@@ -580,12 +585,12 @@ int device_sms()
     return cached_sms;
 }
 
-template <int VPT, bool MOE>
+template <int NC, int VPT, bool MOE, int MINB>
 cudaError_t launch_ring(const BoundaryArgs &a, int stages, size_t smem, int sms,
                         cudaStream_t stream)
 {
-    auto kern = boundary_ring_kernel<VPT, MOE>;
-    const int threads = kRingConsumers + 32;
+    auto kern = boundary_ring_kernel<NC, VPT, MOE, MINB>;
+    const int threads = NC + 32;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
@@ -618,33 +623,44 @@ int pick_vpt(int nvec, int max_threads)
 
 inline int round_warps(int n) { return (n + 31) / 32 * 32; }
 
+// The ring launch for rows of `chunks` chunks of NC vectors.  Stages: as many as fit beside the
+// parked weights in this CTA's share of the SM's 228 KB of shared memory (less 3 KB for the
+// static arrays and the per-CTA reserve), between 2 and 16; 2 for the MoE variant, whose
+// stages hold K + 1 slices.
+template <int NC, bool MOE, int MINB>
+cudaError_t launch_ring_chunks(const BoundaryArgs &a, int chunks, int sms, cudaStream_t stream)
+{
+    const size_t stage = (size_t)((MOE ? a.K : 1) + 1) * NC * 16;
+    const size_t weights = (size_t)2 * chunks * NC * 16;
+    const size_t budget = (size_t)228 * 1024 / MINB - 3 * 1024;
+    int stages = MOE ? 2
+                     : (int)((budget > weights + kRingHeader ? budget - weights - kRingHeader : 0) /
+                             stage);
+    stages = stages < 2 ? 2 : (stages > kRingMaxStages ? kRingMaxStages : stages);
+    const size_t smem = kRingHeader + stages * stage + weights;
+    switch (chunks) {
+    case 1: return launch_ring<NC, 1, MOE, MINB>(a, stages, smem, sms, stream);
+    case 2: return launch_ring<NC, 2, MOE, MINB>(a, stages, smem, sms, stream);
+    case 3: return launch_ring<NC, 3, MOE, MINB>(a, stages, smem, sms, stream);
+    case 4: return launch_ring<NC, 4, MOE, MINB>(a, stages, smem, sms, stream);
+    case 5: return launch_ring<NC, 5, MOE, MINB>(a, stages, smem, sms, stream);
+    case 6: return launch_ring<NC, 6, MOE, MINB>(a, stages, smem, sms, stream);
+    case 7: return launch_ring<NC, 7, MOE, MINB>(a, stages, smem, sms, stream);
+    default: return launch_ring<NC, 8, MOE, MINB>(a, stages, smem, sms, stream);
+    }
+}
+
 template <bool MOE>
 cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
 {
     const int nvec = a.H / 8;
     const int sms = device_sms();
     // Many rows (and rows of at most 8 chunks): the persistent warp-specialised TMA ring.
-    const int chunks = (nvec + kRingConsumers - 1) / kRingConsumers;
-    if (a.T >= 4 * (int64_t)sms && chunks <= 8) {
-        const size_t stage = (size_t)((MOE ? a.K : 1) + 1) * kRingConsumers * 16;
-        const size_t weights = (size_t)2 * chunks * kRingConsumers * 16;
-        // stages: about 32 KB per CTA for the plain boundary (4 CTAs per SM); 2 for the MoE
-        // variant, whose stages hold K + 1 slices, so that its weights fit beside them at 3 CTAs
-        // per SM; at most 16
-        int stages = MOE ? 2 : (int)((32 * 1024) / stage);
-        stages = stages < 2 ? 2 : (stages > kRingMaxStages ? kRingMaxStages : stages);
-        const size_t smem = kRingHeader + stages * stage + weights;
-        switch (chunks) {
-        case 1: return launch_ring<1, MOE>(a, stages, smem, sms, stream);
-        case 2: return launch_ring<2, MOE>(a, stages, smem, sms, stream);
-        case 3: return launch_ring<3, MOE>(a, stages, smem, sms, stream);
-        case 4: return launch_ring<4, MOE>(a, stages, smem, sms, stream);
-        case 5: return launch_ring<5, MOE>(a, stages, smem, sms, stream);
-        case 6: return launch_ring<6, MOE>(a, stages, smem, sms, stream);
-        case 7: return launch_ring<7, MOE>(a, stages, smem, sms, stream);
-        default: return launch_ring<8, MOE>(a, stages, smem, sms, stream);
-        }
-    }
+    constexpr int NC = MOE ? kMoeConsumers : kPlainConsumers;
+    const int chunks = (nvec + NC - 1) / NC;
+    if (a.T >= 4 * (int64_t)sms && chunks <= 8)
+        return launch_ring_chunks<NC, MOE, MOE ? kMoeCtasPerSm : kPlainCtasPerSm>(a, chunks, sms,
+                                                                                 stream);
     // Few rows (or very wide rows): one CTA per row straight from memory.
     const bool small = a.T < 2 * (int64_t)sms;
     const int max_threads = small ? 1024 : (MOE ? 320 : 256);
@@ -705,6 +721,26 @@ cudaError_t launch_copy_timeout_selftest(unsigned long long limit_ns, cudaStream
     copy_timeout_selftest_kernel<<<1, 64, 0, stream>>>(limit_ns);
     return cudaGetLastError();
 }
+
+unsigned int *fault_word_device()
+{
+    static std::mutex mu;
+    static int cached_dev = -1;
+    static unsigned int *cached_ptr = nullptr;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev != cached_dev) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess)
+            return nullptr;
+        cached_ptr = static_cast<unsigned int *>(p);
+        cached_dev = dev;
+    }
+    return cached_ptr;
+}
+
+int device_sm_count() { return device_sms(); }
 
 cudaError_t read_fault_word(unsigned int *value, bool clear)
 {

@@ -57,10 +57,27 @@ def test_head_counts(kind, nq, nk):
 
 
 @pytest.mark.parametrize("kind", ["rope", "ssmax"])
-def test_views_into_packed_qkv_gate_projection(kind):
+@pytest.mark.parametrize("T,nq,nk", [(609, 48, 8), (1999, 48, 8), (1001, 3, 2), (1001, 1, 0),
+                                     (1001, 0, 1), (1001, 64, 8)])
+def test_many_tokens_ragged_tails(kind, T, nq, nk):
+    # From 4 x 152 tokens on, the persistent kernel: two-token tiles prefetched into shared
+    # memory a tile ahead, CTAs looping over several tiles, a one-token last tile for odd T.
+    # 64 + 8 heads do not fit its double buffer and take the direct kernel instead.
+    c = bi.attn_qk_case(T=T, n_q=nq, n_kv=nk, seed=T + nq + nk)
+    q = dev(c["q"]) if nq else torch.empty((T, 0, D), dtype=torch.bfloat16, device="cuda")
+    k = dev(c["k"]) if nk else torch.empty((T, 0, D), dtype=torch.bfloat16, device="cuda")
+    q, k = run_qk(kind, c, q=q, k=k)
+    wq, wk = oracle_qk(kind, c)
+    assert_bf16_close(u16(q), wq, what=f"{kind} q T={T} {nq}/{nk}")
+    assert_bf16_close(u16(k), wk, what=f"{kind} k T={T} {nq}/{nk}")
+    assert rsn.beam_device_faults() == 0
+
+
+@pytest.mark.parametrize("kind", ["rope", "ssmax"])
+@pytest.mark.parametrize("T", [37, 1001])
+def test_views_into_packed_qkv_gate_projection(kind, T):
     # One packed [T, (48 + 8 + 8) * 128 + 48 * 128] projection output (Q | K | V | gate):
     # Q and K are row-strided views; V and the gate columns must stay untouched.
-    T = 37
     c = bi.attn_qk_case(T=T, seed=21)
     g = bi.rng(22)
     v = bi.to_bf16(bi.normal(g, (T, 8 * D)))
@@ -175,7 +192,7 @@ def test_zero_tokens():
 
 
 @pytest.mark.parametrize("kind", ["rope", "ssmax"])
-@pytest.mark.parametrize("T", [3, 400])
+@pytest.mark.parametrize("T", [3, 400, 1001])
 def test_near_tie_head_sums(kind, T):
     # heads whose sum of squares sits at or just above an FP32 rounding boundary: the RoPE kernel
     # rounds its head sums exactly (its rotation can cancel), so its outputs are bit-identical;

@@ -87,7 +87,7 @@ def check_caches(kind, c, kv, fp8, got, k_scale=1.0, v_scale=1.0, what=""):
 
 @pytest.mark.parametrize("kind", ["rope", "ssmax"])
 @pytest.mark.parametrize("fp8", [False, True])
-@pytest.mark.parametrize("T,mode", [(128, "uniform"), (2048, "contiguous")])
+@pytest.mark.parametrize("T,mode", [(128, "uniform"), (2048, "contiguous"), (1999, "uniform")])
 def test_qk_kv_configs(kind, fp8, T, mode):
     lib()
     c = bi.attn_qk_case(T=T, seed=T + 1, pos_mode=mode)
@@ -104,9 +104,9 @@ def test_fp8_scales_power_of_two_and_general(kind, k_scale, v_scale):
     check_caches(kind, c, kv, True, got, k_scale, v_scale, what=f"scales {k_scale},{v_scale}")
 
 
+@pytest.mark.parametrize("T", [9, 1001])
 @pytest.mark.parametrize("nq,nk", [(1, 1), (3, 2), (64, 8), (0, 3), (5, 0)])
-def test_head_counts_with_cache(nq, nk):
-    T = 9
+def test_head_counts_with_cache(nq, nk, T):
     c = bi.attn_qk_case(T=T, n_q=nq, n_kv=nk, seed=nq * 7 + nk)
     kv = bi.kv_cache_case(T=T, n_kv=nk, seed=3, pad_frac=0.2, oob_frac=0.1)
     q = dev(c["q"]) if nq else torch.empty((T, 0, D), dtype=torch.bfloat16, device="cuda")
@@ -117,9 +117,9 @@ def test_head_counts_with_cache(nq, nk):
         check_caches("rope", c, kv, fp8, got, what=f"{nq}/{nk} fp8={fp8}")
 
 
-def test_views_into_packed_qkv_projection():
+@pytest.mark.parametrize("T", [33, 1001])
+def test_views_into_packed_qkv_projection(T):
     # Q, K and V as row-strided views of one packed [T, (48 + 8 + 8) * 128] projection output
-    T = 33
     c = bi.attn_qk_case(T=T, seed=8)
     kv = bi.kv_cache_case(T=T, seed=9)
     packed = torch.cat([c["q"].reshape(T, -1), c["k"].reshape(T, -1), kv["v"].reshape(T, -1)],
