@@ -13,16 +13,20 @@
 // expert rows) and h once and writes h' and y once; the norm weights come from L1/L2 (rows
 // kernel) or are parked once per CTA in shared memory (ring kernel).
 //
-// Two layouts, same arithmetic (boundary_chain):
+// Three layouts, same arithmetic (boundary_chain):
 //  * rows kernel (few tokens, e.g. batch-1 decode): one CTA per token row; each thread owns VPT
 //    16-byte vectors at vector indices tid + i * blockDim.x and loads them straight from memory.
-//  * ring kernel (many tokens): a persistent grid (SM count x CTAs per SM) with warp
-//    specialisation: one producer warp issues bulk TMA copies (cp.async.bulk, completion on
-//    "full" mbarriers) of each row's inputs in chunks of 128 vectors -- the x chunk or the K
-//    expert chunks, and the h chunk -- into a ring of shared-memory stages, and four consumer
+//  * prefetch kernel (many tokens, plain boundary): a persistent grid of 4-warp CTAs, each with
+//    two row buffers in shared memory that one of its threads refills with bulk TMA copies
+//    (cp.async.bulk, completion on an mbarrier) two rows ahead, right after the first block
+//    reduction of the row that leaves the buffer.
+//  * ring kernel (many tokens, MoE variant): a persistent grid with warp specialisation: one
+//    producer warp issues bulk TMA copies of each row's inputs in chunks of 128 vectors -- the K
+//    expert chunks and the h chunk -- into a ring of shared-memory stages, and four consumer
 //    warps reduce and finish the rows, releasing each stage on an "empty" mbarrier as soon as
-//    they have read it.  Only 4 warps share a row, so the two block reductions per row stay
-//    cheap, and several CTAs fit on an SM.
+//    they have read it.
+// Only 4 warps share a row, so the two block reductions per row stay cheap, and several CTAs fit
+// on an SM.
 // The row stays in registers as packed BF16 between the two block reductions; element math runs
 // on packed FP32 pairs (beam_f32x2.cuh) with the same IEEE roundings as the scalar definition.
 
@@ -425,12 +429,10 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
 constexpr int kRingHeader = 256;  // 2 x up to 16 mbarriers
 constexpr int kRingMaxStages = 16;
 
-// Ring shapes: consumer threads per CTA and CTAs per SM.  The MoE variant's stages hold K + 1
-// slices, so it keeps slices small (4 consumer warps) at 3 CTAs per SM.
+// Ring shape of the MoE variant: its stages hold K + 1 slices, so it keeps slices small (4
+// consumer warps) at 3 CTAs per SM.
 constexpr int kMoeConsumers = 128;
 constexpr int kMoeCtasPerSm = 3;
-constexpr int kPlainConsumers = 128;
-constexpr int kPlainCtasPerSm = 3;
 
 template <int NC, int VPT, bool MOE, int MINB>
 __global__ void __launch_bounds__(NC + 32, MINB)
@@ -569,6 +571,107 @@ __global__ void __launch_bounds__(NC + 32, MINB)
         atomicOr(&g_fault_word, kFaultCopyTimeout);
 }
 
+// ---- prefetch kernel: persistent, every warp a consumer ---------------------------------------
+//
+// The plain boundary without a producer warp: a CTA of NC = 128 threads keeps NBUF row buffers
+// in shared memory (x then h, nvec vectors each), filled by two bulk copies per row with one
+// "full" mbarrier per buffer.  Thread t owns vectors t + c * NC of a row.  Right after the first
+// block reduction of a row -- when every thread has read the row out of its buffer, since the
+// reduction's barrier follows the reads -- thread 0 refills that buffer with the row NBUF rows
+// ahead, so the copies fly during the rest of the row's chain and the next rows'.  With the norm
+// weights parked in shared memory too (WSMEM), a row buffer and the weights take 40 KB for
+// H = 5120, and 4 CTAs of 4 warps fit on an SM at up to 128 registers a thread.
+
+template <int VPT, int NBUF, bool WSMEM>
+__global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs a)
+{
+    constexpr int NC = 128;
+    extern __shared__ __align__(128) unsigned char dyn[];
+    __shared__ __align__(8) uint64_t full[NBUF];
+    __shared__ Sum2 red[32];
+    __shared__ ExactSlot xred[32];
+    __shared__ float pred[32];
+    __shared__ int fail;
+    const int nvec = a.H >> 3;
+    const int tid = threadIdx.x;
+    const uint32_t tbytes = (uint32_t)nvec * 16u;                  // one tensor's row
+    const size_t buf_bytes = (size_t)2 * VPT * NC * 16;           // x and h slots of a buffer
+    uint4 *wsm = reinterpret_cast<uint4 *>(dyn + (size_t)NBUF * buf_bytes);  // [2][VPT][NC]
+    const int64_t first = blockIdx.x;
+    const int64_t stride = gridDim.x;
+    const int64_t my_rows = first < a.T ? (a.T - first + stride - 1) / stride : 0;
+
+    auto issue = [&](int64_t row, int b) {
+        unsigned char *dst = dyn + (size_t)b * buf_bytes;
+        mbar_arrive_expect_tx(&full[b], 2u * tbytes);
+        bulk_g2s(dst, (const char *)a.x_in + (size_t)row * 2 * a.H, tbytes, &full[b]);
+        bulk_g2s(dst + (size_t)VPT * NC * 16, (const char *)a.h_in + (size_t)row * 2 * a.H,
+                 tbytes, &full[b]);
+    };
+
+    pdl_launch_dependents();
+    if (tid == 0) {
+        for (int b = 0; b < NBUF; ++b)
+            mbar_init(&full[b], 1);
+        fail = 0;
+        fence_mbar_init();
+    }
+    if constexpr (WSMEM) {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+            wsm[i * NC + tid] = weight_vec(a.w_post, tid + i * NC, nvec);
+            wsm[(VPT + i) * NC + tid] = weight_vec(a.w_pre, tid + i * NC, nvec);
+        }
+    }
+    __syncthreads();
+    pdl_wait();
+    if (tid == 0)
+        for (int b = 0; b < NBUF && b < my_rows; ++b)
+            issue(first + b * stride, b);
+
+    for (int64_t i = 0; i < my_rows; ++i) {
+        const int64_t row = first + i * stride;
+        const int b = (int)(i % NBUF);
+        (void)mbar_wait_or_fail(&full[b], (uint32_t)((i / NBUF) & 1), &fail);
+        const unsigned char *buf = dyn + (size_t)b * buf_bytes;
+        uint4 xv[VPT], hv[VPT];
+#pragma unroll
+        for (int c = 0; c < VPT; ++c) {
+            const int v = tid + c * NC;
+            if (v < nvec) {
+                xv[c] = *reinterpret_cast<const uint4 *>(buf + 16 * v);
+                hv[c] = *reinterpret_cast<const uint4 *>(buf + (size_t)VPT * NC * 16 + 16 * v);
+            } else {
+                xv[c] = make_uint4(0u, 0u, 0u, 0u);
+                hv[c] = xv[c];
+            }
+        }
+        const bool refill = i + NBUF < my_rows;
+        boundary_chain<VPT>(
+            a, row, xv, hv,
+            [&](int k) {
+                return WSMEM ? wsm[k * NC + tid] : weight_vec(a.w_post, tid + k * NC, nvec);
+            },
+            [&](int k) {
+                return WSMEM ? wsm[(VPT + k) * NC + tid] : weight_vec(a.w_pre, tid + k * NC, nvec);
+            },
+            red, xred, pred, NC, false, [&] {
+                if (tid == 0 && refill)
+                    issue(row + NBUF * stride, b);
+            });
+    }
+    // Every copy issued was waited for above unless a wait gave up; then make sure none is still
+    // landing before the CTA leaves (bounded), and raise the fault word.
+    if (tid == 0 && fail) {
+        for (int b = 0; b < NBUF; ++b) {
+            const int64_t uses = my_rows > b ? (my_rows - b + NBUF - 1) / NBUF : 0;
+            if (uses > 0)
+                (void)mbar_wait(&full[b], (uint32_t)((uses - 1) & 1));
+        }
+        atomicOr(&g_fault_word, kFaultCopyTimeout);
+    }
+}
+
 // ---- launch ----------------------------------------------------------------------------------
 
 int device_sms()
@@ -650,17 +753,64 @@ cudaError_t launch_ring_chunks(const BoundaryArgs &a, int chunks, int sms, cudaS
     }
 }
 
+// Row buffers and whether the weights are parked in shared memory, for the prefetch kernel: two
+// buffers and the weights (60 KB for H = 5120, 3 CTAs per SM) were the fastest of the shapes
+// measured; without the weights in shared memory the long-latency weight loads inside the chain
+// cost 15%.
+constexpr int kPfBuffers = 2;
+constexpr bool kPfWeightsInSmem = true;
+
+template <int VPT>
+cudaError_t launch_pf_vpt(const BoundaryArgs &a, int sms, cudaStream_t stream)
+{
+    auto kern = boundary_pf_kernel<VPT, kPfBuffers, kPfWeightsInSmem>;
+    const size_t smem = (size_t)kPfBuffers * 2 * VPT * 128 * 16 +
+                        (kPfWeightsInSmem ? (size_t)2 * VPT * 128 * 16 : 0);
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, smem);
+    if (e != cudaSuccess)
+        return e;
+    if (per_sm < 1)
+        return cudaErrorInvalidConfiguration;
+    const int64_t slots = (int64_t)sms * per_sm;
+    const unsigned grid = (unsigned)(a.T < slots ? a.T : slots);
+    e = launch_pdl(kern, dim3(grid), dim3(128), smem, stream, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_pf(const BoundaryArgs &a, int chunks, int sms, cudaStream_t stream)
+{
+    switch (chunks) {
+    case 1: return launch_pf_vpt<1>(a, sms, stream);
+    case 2: return launch_pf_vpt<2>(a, sms, stream);
+    case 3: return launch_pf_vpt<3>(a, sms, stream);
+    case 4: return launch_pf_vpt<4>(a, sms, stream);
+    case 5: return launch_pf_vpt<5>(a, sms, stream);
+    case 6: return launch_pf_vpt<6>(a, sms, stream);
+    case 7: return launch_pf_vpt<7>(a, sms, stream);
+    default: return launch_pf_vpt<8>(a, sms, stream);
+    }
+}
+
 template <bool MOE>
 cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
 {
     const int nvec = a.H / 8;
     const int sms = device_sms();
-    // Many rows (and rows of at most 8 chunks): the persistent warp-specialised TMA ring.
-    constexpr int NC = MOE ? kMoeConsumers : kPlainConsumers;
-    const int chunks = (nvec + NC - 1) / NC;
-    if (a.T >= 4 * (int64_t)sms && chunks <= 8)
-        return launch_ring_chunks<NC, MOE, MOE ? kMoeCtasPerSm : kPlainCtasPerSm>(a, chunks, sms,
-                                                                                 stream);
+    // Many rows (and rows of at most 8 chunks of 128 vectors): the persistent kernels, the
+    // prefetch kernel for the plain boundary and the warp-specialised TMA ring for the MoE
+    // variant.
+    const int chunks = (nvec + 127) / 128;
+    if (a.T >= 4 * (int64_t)sms && chunks <= 8) {
+        if constexpr (MOE)
+            return launch_ring_chunks<kMoeConsumers, true, kMoeCtasPerSm>(a, chunks, sms, stream);
+        else
+            return launch_pf(a, chunks, sms, stream);
+    }
     // Few rows (or very wide rows): one CTA per row straight from memory.
     const bool small = a.T < 2 * (int64_t)sms;
     const int max_threads = small ? 1024 : (MOE ? 320 : 256);

@@ -54,6 +54,8 @@ def test_single_boundary_config():
     # enough rows for the persistent TMA ring (>= 4 rows per SM), ragged and maximum H
     (700, 5120, 13), (613, 5128, 2), (1000, 16384, 104), (2000, 8, 3), (640, 24, 77),
     (650, 5120, 5000),
+    # several rows per CTA through the row buffers, ragged rows
+    (3001, 1032, 8), (1999, 5120, 21),
 ])
 def test_shapes(T, H, n):
     c = bi.boundary_case(T=T, H=H, n=n, seed=T + H, outlier_frac=0.05, outlier_mult=16.0,
