@@ -12,9 +12,9 @@
 //    "混合注意力与输出门控" and the kernel-fusion paragraph (bias add, sigmoid, multiply fused).
 //
 // Q/K layout: each quad of lanes owns one (token, head) item of 128 elements.  Without a KV cache
-// a CTA of 256 threads takes tiles of 4 tokens, two items per quad per pass, all loads of a pass
-// issued before any arithmetic (qk_norm_kernel); with a cache, a persistent kernel prefetches
-// 2-token tiles into shared memory with bulk copies a tile ahead (qk_ring_kernel).  The
+// a CTA of 256 threads takes tiles of 8 (RoPE) or 4 (SSMax) tokens, one item per quad per pass,
+// its loads issued before any arithmetic (qk_norm_kernel); with a cache, a persistent kernel
+// prefetches 2-token tiles into shared memory with bulk copies a tile ahead (qk_ring_kernel).  The
 // per-token factors (64 cos/sin pairs, or the SSMax scale) are computed once per token into
 // shared memory.  cos/sin are the FP32 roundings of the exact values of the FP32 angle
 // (beam_sincos.cuh), so the rotation matches the oracle bit for bit even where its two products
@@ -36,7 +36,7 @@ constexpr int kHeadDim = 128;
 constexpr int kHalf = kHeadDim / 2;
 constexpr int kQkThreads = 256;
 constexpr int kSlots = kQkThreads / 4;  // one head per quad of lanes
-constexpr int kIPP = 2;                 // heads per quad per pass, loads issued together
+constexpr int kIPP = 1;                 // heads per quad per pass, loads issued together
 
 struct RopeTable {
     float inv_freq[kHalf];  // fp32(theta^(-2i/128)), formed on the host in double
@@ -303,12 +303,12 @@ __device__ __forceinline__ char *item_row(const QkArgs &a, int64_t t, int hd, in
     return (char *)a.v + 2 * (t * a.v_stride + (int64_t)(hd - nqk) * kHeadDim);  // only read
 }
 
-// Direct kernel (few tokens): a CTA of 256 threads takes tiles of TT tokens, each quad two items
-// per pass, all loads of a pass issued (straight from global memory) before any arithmetic; the
-// tile's factors are computed while the first loads are in flight.  The Q and K norm weights are
-// held in shared memory as FP32.
+// Direct kernel: a CTA of 256 threads takes tiles of TT tokens, each quad kIPP items per pass,
+// all loads of a pass issued (straight from global memory) before any arithmetic; the tile's
+// factors are computed while the first loads are in flight.  The Q and K norm weights are held
+// in shared memory as FP32.
 template <bool ROPE, int TT, bool KV>
-__global__ void __launch_bounds__(kQkThreads, 3) qk_norm_kernel(const QkArgs a, const RopeTable tab)
+__global__ void __launch_bounds__(kQkThreads, 4) qk_norm_kernel(const QkArgs a, const RopeTable tab)
 {
     __shared__ __align__(16) float cs[2][TT][kHalf];  // double-buffered by tile parity
     __shared__ __align__(16) float sn[2][TT][kHalf];
@@ -628,11 +628,13 @@ cudaError_t launch_qk(const QkArgs &a_in, cudaStream_t stream)
             return e != cudaSuccess ? e : cudaGetLastError();
         }
     }
-    // Without the cache the direct kernel is the faster one: its 4-token tiles keep two heads'
-    // loads in flight per quad and need no barrier per tile.  Few tokens: one token per CTA
-    // spreads them over more SMs.
+    // Without the cache the direct kernel is the faster one: 4 CTAs of 8 warps on an SM, one
+    // head per quad per pass, and no barrier per tile.  Tiles of 8 tokens for RoPE (each thread
+    // then forms two cos/sin pairs per tile), 4 for SSMax: the faster of the sizes measured.
+    // Few tokens: one token per CTA spreads them over more SMs.
+    constexpr int TT = ROPE ? 8 : 4;
     if (many)
-        e = launch_pdl(qk_norm_kernel<ROPE, 4, KV>, dim3(grid_for((a.T + 3) / 4)),
+        e = launch_pdl(qk_norm_kernel<ROPE, TT, KV>, dim3(grid_for((a.T + TT - 1) / TT)),
                        dim3(kQkThreads), 0, stream, a, tab);
     else
         e = launch_pdl(qk_norm_kernel<ROPE, 1, KV>, dim3(grid_for(a.T)), dim3(kQkThreads), 0,
