@@ -11,10 +11,11 @@
 //  * Sigmoid output gate: [vLLM] "Attention", bullet "Sigmoid-Output-Gate"; [SGL]
 //    "混合注意力与输出门控" and the kernel-fusion paragraph (bias add, sigmoid, multiply fused).
 //
-// Q/K layout: each quad of lanes owns one (token, head) item of 128 elements.  Without a KV cache
-// a CTA of 256 threads takes tiles of 8 (RoPE) or 4 (SSMax) tokens, one item per quad per pass,
-// its loads issued before any arithmetic (qk_norm_kernel); with a cache, a persistent kernel
-// prefetches 2-token tiles into shared memory with bulk copies a tile ahead (qk_ring_kernel).  The
+// Q/K layout: each quad of lanes owns one (token, head) item of 128 elements.  A CTA of 256
+// threads takes tiles of 8 (RoPE) or 4 (SSMax) tokens, one item per quad per pass.  The direct
+// kernel (qk_norm_kernel) loads a pass straight into registers; the staged kernel
+// (qk_stage_kernel) copies the next pass into shared memory (cp.async) while it works on this
+// one.  The
 // per-token factors (64 cos/sin pairs, or the SSMax scale) are computed once per token into
 // shared memory.  cos/sin are the FP32 roundings of the exact values of the FP32 angle
 // (beam_sincos.cuh), so the rotation matches the oracle bit for bit even where its two products
@@ -118,12 +119,10 @@ __device__ __forceinline__ void cache_store(void *cache, int64_t e, uint4 o, int
 // A quad of lanes owns one (token, head) item of 128 elements: lane q holds the 16-byte vectors
 // q + 4 k (k = 0..3) of the head, so the rotation partners (element i < 64 and i + 64, i.e.
 // vectors q + 4 k and q + 4 (k + 2)) sit in the same lane, and the head's sum of squares needs a
-// two-step butterfly over the quad.  Register jj of the lane holds vector q + 4 (jj ^ sw): the
-// persistent kernel flips the order on odd quads (sw = 1) so that a warp's shared-memory reads
-// spread over all banks; the direct kernel uses sw = 0.  With a KV cache the items also include
-// the V heads: their rows go to the V cache as they are, and the K rows go to the K cache as they
-// are stored (after the norm and rotation).  Quads of one warp may then take different paths, so
-// every shuffle is masked to its quad.
+// two-step butterfly over the quad.  With a KV cache the items also include the V heads: their
+// rows go to the V cache as they are, and the K rows go to the K cache as they are stored (after
+// the norm and rotation).  Quads of one warp may then take different paths, so every shuffle is
+// masked to its quad.
 
 // The per-token factors of one tile: 64 cos/sin pairs per token (RoPE), or the SSMax query
 // scale.  cos/sin are the FP32 roundings of the exact values of the FP32 angle.
@@ -162,7 +161,7 @@ __device__ __forceinline__ void tile_factors(const QkArgs &a, const RopeTable &t
 // warp call it together.
 template <bool ROPE, bool KV>
 __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], char *row, int tt,
-                                        int hd, int64_t t0, int q, int sw, unsigned qmask,
+                                        int hd, int64_t t0, int q, unsigned qmask,
                                         const float (&wsm)[2][kHeadDim], const float *cst,
                                         const float *snt, float sq, f2 nz)
 {
@@ -180,7 +179,7 @@ __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], ch
             const int64_t e0 = (cslot * a.n_kv + (hd - nqk)) * kHeadDim;
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
-                cache_store(a.v_cache, e0 + 8 * (q + 4 * (jj ^ sw)), v[jj], a.cache_mode,
+                cache_store(a.v_cache, e0 + 8 * (q + 4 * jj), v[jj], a.cache_mode,
                             a.v_scale, a.v_inv, a.v_pow2);
         }
         return;
@@ -243,7 +242,7 @@ __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], ch
     f2 qh[4][4];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
-        const int e0 = 8 * (q + 4 * (jj ^ sw));
+        const int e0 = 8 * (q + 4 * jj);
 #pragma unroll
         for (int pp = 0; pp < 4; ++pp) {
             const f2 w = *reinterpret_cast<const f2 *>(&wrow[e0 + 2 * pp]);
@@ -254,12 +253,12 @@ __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], ch
     if constexpr (ROPE) {
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
-            const int i0 = 8 * (q + 4 * (jj ^ sw));  // first-half element index (< 64)
+            const int i0 = 8 * (q + 4 * jj);  // first-half element index (< 64)
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp) {
                 const f2 c = *reinterpret_cast<const f2 *>(&cst[i0 + 2 * pp]);
                 const f2 sv = *reinterpret_cast<const f2 *>(&snt[i0 + 2 * pp]);
-                const f2 lo = qh[jj][pp], hi = qh[jj + 2][pp];  // (jj + 2) ^ sw = (jj ^ sw) + 2
+                const f2 lo = qh[jj][pp], hi = qh[jj + 2][pp];
                 // out_i = q_i c - q_{i+64} s;  out_{i+64} = q_{i+64} c + q_i s, each product
                 // rounded.  A packed product that feeds a packed add is fused into one FMA by the
                 // compiler, so each product is formed as fma(x, y, nz) with nz = -0 (the same
@@ -284,7 +283,7 @@ __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], ch
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp)
                 word(o, pp) = narrow(out[jj][pp]);
-            const int vi = q + 4 * (jj ^ sw);
+            const int vi = q + 4 * jj;
             st_global(row + 16 * vi, o);
             if (KV && cslot >= 0)  // a K item: the stored K' also into the K cache
                 cache_store(a.k_cache, e0 + 8 * vi, o, a.cache_mode, a.k_scale, a.k_inv,
@@ -367,140 +366,103 @@ __global__ void __launch_bounds__(kQkThreads, 4) qk_norm_kernel(const QkArgs a, 
             }
 #pragma unroll
             for (int m = 0; m < kIPP; ++m)
-                qk_item<ROPE, KV>(a, v[m], row[m], tok[m], head[m], t0, q, 0, qmask, wsm,
+                qk_item<ROPE, KV>(a, v[m], row[m], tok[m], head[m], t0, q, qmask, wsm,
                                   cs[buf][tok[m]], sn[buf][tok[m]],
                                   ROPE ? 0.0f : scale_q[buf][tok[m]], splat(tab.neg_zero));
         }
     }
 }
 
-// Persistent kernel (many tokens): CTAs loop over tiles of kRingTT tokens.  One thread issues
-// bulk copies (TMA) of a tile's Q, K (and V) rows into one of two shared-memory buffers a tile
-// ahead, so the next tile's reads are in flight while the warps work on this one; the factors of
-// the next tile are computed at the same point.  A tile's items are then read from shared memory,
-// quad by quad, and finished as in the direct kernel.  The block has one quad per two items of a
-// tile (at most 256 threads), so every quad has the same work between the per-tile barriers:
-// 224 threads for 2 x 56 heads, 256 with the V heads.  Every
-// wait on a copy is bounded (beam_tma.cuh); a CTA that gives up raises the fault word.
-constexpr int kRingTT = 2;
-
-template <bool ROPE, bool KV>
-__device__ __forceinline__ void issue_tile(const QkArgs &a, int64_t tile, int nheads,
-                                           unsigned char *dst, uint64_t *bar)
+// 16-byte asynchronous copy global -> shared (cp.async, L2 only), and its group bookkeeping.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
 {
-    const int64_t t0 = tile * kRingTT;
-    const int nt = (int)(a.T - t0 < kRingTT ? a.T - t0 : kRingTT);
-    const int nqk = a.n_q + a.n_kv;
-    mbar_arrive_expect_tx(bar, (uint32_t)(nt * nheads) * 256u);
-    for (int tt = 0; tt < nt; ++tt) {
-        const int64_t t = t0 + tt;
-        unsigned char *d = dst + (size_t)tt * nheads * 256;
-        if (a.n_q > 0)
-            bulk_g2s(d, (const char *)a.q + 2 * t * a.q_stride, (uint32_t)a.n_q * 256u, bar);
-        if (a.n_kv > 0) {
-            bulk_g2s(d + (size_t)a.n_q * 256, (const char *)a.k + 2 * t * a.k_stride,
-                     (uint32_t)a.n_kv * 256u, bar);
-            if (KV)
-                bulk_g2s(d + (size_t)nqk * 256, (const char *)a.v + 2 * t * a.v_stride,
-                         (uint32_t)a.n_kv * 256u, bar);
-        }
-    }
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem)
+                 : "memory");
 }
 
-template <bool ROPE, bool KV>
-__global__ void __launch_bounds__(kQkThreads, 3)
-    qk_ring_kernel(const QkArgs a, const RopeTable tab)
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most one of this thread's copy groups is still pending.
+__device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+
+// Staged kernel (many tokens): the direct kernel's tiles, one head per quad per pass, with each
+// thread's four vectors of the next pass copied into shared memory (cp.async) while it works on
+// this pass, so two passes' reads are in flight per thread without holding registers for them.
+// A thread reads back only what it copied itself, so no barrier guards the staging buffers;
+// [pass parity][vector][thread] keeps a warp's reads of one vector contiguous (no bank
+// conflicts).
+template <bool ROPE, int TT, bool KV>
+__global__ void __launch_bounds__(kQkThreads, 4) qk_stage_kernel(const QkArgs a, const RopeTable tab)
 {
-    constexpr int TT = kRingTT;
-    extern __shared__ __align__(128) unsigned char qbuf[];  // [2][TT * nheads * 256 bytes]
-    __shared__ __align__(8) uint64_t full[2];
-    __shared__ __align__(16) float cs[2][TT][kHalf];
+    __shared__ __align__(16) float cs[2][TT][kHalf];  // double-buffered by tile parity
     __shared__ __align__(16) float sn[2][TT][kHalf];
     __shared__ float scale_q[2][TT];
     __shared__ __align__(16) float wsm[2][kHeadDim];
-    __shared__ int fail;
+    __shared__ __align__(16) uint4 stage[2][4][kQkThreads];
     const int nqk = a.n_q + a.n_kv;
     const int nheads = nqk + (KV ? a.n_kv : 0);
-    const size_t tile_bytes = (size_t)TT * nheads * 256;
     const unsigned qmask = KV ? 0xfu << (threadIdx.x & 28) : 0xffffffffu;
     const int tid = threadIdx.x;
     const int q = tid & 3;
     const int slot = tid >> 2;
-    const int nslots = blockDim.x >> 2;  // quads: the launch sizes the block to the tile
-    const int sw = slot & 1;
     pdl_launch_dependents();
-    for (int i = tid; i < 2 * kHeadDim; i += blockDim.x) {
-        const int which = i >> 7, e = i & 127;
+    {
+        const int which = tid >> 7, e = tid & 127;
         const bool have = which == 0 ? a.n_q > 0 : a.n_kv > 0;
         const uint16_t *w = (const uint16_t *)(which == 0 ? a.wq : a.wk);
         wsm[which][e] = have ? __uint_as_float((uint32_t)w[e] << 16) : 0.0f;
     }
-    if (tid == 0) {
-        mbar_init(&full[0], 1);
-        mbar_init(&full[1], 1);
-        fail = 0;
-        fence_mbar_init();
-    }
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     const int64_t ntiles = (a.T + TT - 1) / TT;
-    const int64_t first = blockIdx.x, stride = gridDim.x;
+    int buf = 0;
     __syncthreads();
     pdl_wait();
-    uint32_t uses[2] = {0u, 0u};  // copies issued into each buffer (thread 0)
-    if (first < ntiles) {
-        if (tid == 0) {
-            issue_tile<ROPE, KV>(a, first, nheads, qbuf, &full[0]);
-            uses[0] = 1;
-        }
-        const int64_t t0 = first * TT;
-        tile_factors<ROPE, TT>(a, tab, t0, (int)(a.T - t0 < TT ? a.T - t0 : TT), cs[0], sn[0],
-                               scale_q[0]);
-    }
-    int k = 0;
-    for (int64_t tile = first; tile < ntiles; tile += stride, ++k) {
-        const int b = k & 1;
-        __syncthreads();  // tile k - 1 is done: its buffer and factors may be refilled
-        const int64_t next = tile + stride;
-        if (next < ntiles) {
-            if (tid == 0) {
-                issue_tile<ROPE, KV>(a, next, nheads, qbuf + (b ^ 1) * tile_bytes, &full[b ^ 1]);
-                ++uses[b ^ 1];
-            }
-            const int64_t tn = next * TT;
-            tile_factors<ROPE, TT>(a, tab, tn, (int)(a.T - tn < TT ? a.T - tn : TT), cs[b ^ 1],
-                                   sn[b ^ 1], scale_q[b ^ 1]);
-        }
-        (void)mbar_wait_or_fail(&full[b], (uint32_t)(k >> 1) & 1u, &fail);
+
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, buf ^= 1) {
         const int64_t t0 = tile * TT;
         const int nt = (int)(a.T - t0 < TT ? a.T - t0 : TT);
         const int nitems = nt * nheads;
-        const unsigned char *tb = qbuf + b * tile_bytes;
-        // items j = slot, slot + nslots, ...: read from shared memory one at a time (short
-        // latency); every warp runs the same number of rounds
-        for (int j = slot; j < ((nitems + nslots - 1) / nslots) * nslots; j += nslots) {
-            int tt = 0, hd = j < nitems ? j : 0;  // inactive items map to (0, 0)
-            while (hd >= nheads) {  // at most TT - 1 steps
+        const int npass = (nitems + kSlots - 1) / kSlots;
+        // item of pass p for this quad: token tt and head hd of the tile, or none
+        auto locate = [&](int p, int &tt, int &hd) -> char * {
+            const int j = p * kSlots + slot;
+            tt = 0;
+            hd = j < nitems ? j : 0;
+            while (hd >= nheads) {
                 hd -= nheads;
                 ++tt;
             }
-            char *row = j < nitems ? item_row(a, t0 + tt, hd, nqk) : nullptr;
-            const unsigned char *src = tb + (size_t)(row ? j : 0) * 256;
+            return j < nitems ? item_row(a, t0 + tt, hd, nqk) : nullptr;
+        };
+        auto issue = [&](int p) {
+            int tt, hd;
+            const char *row = locate(p, tt, hd);
+            if (row)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    cp_async16(&stage[p & 1][jj][tid], row + 16 * (q + 4 * jj));
+            cp_async_commit();
+        };
+        issue(0);
+        for (int p = 0; p < npass; ++p) {
+            if (p + 1 < npass)
+                issue(p + 1);
+            else
+                cp_async_commit();  // an empty group keeps "all but the newest" meaning pass p
+            if (p == 0) {  // the tile's factors, while the first copies fly
+                tile_factors<ROPE, TT>(a, tab, t0, nt, cs[buf], sn[buf], scale_q[buf]);
+                __syncthreads();
+            }
+            cp_async_wait_one();
+            int tt, hd;
+            char *row = locate(p, tt, hd);
             uint4 v[4];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
-                v[jj] = row ? *reinterpret_cast<const uint4 *>(src + 16 * (q + 4 * (jj ^ sw)))
-                            : zero;
-            qk_item<ROPE, KV>(a, v, row, tt, hd, t0, q, sw, qmask, wsm, cs[b][tt], sn[b][tt],
-                              ROPE ? 0.0f : scale_q[b][tt], splat(tab.neg_zero));
+                v[jj] = row ? stage[p & 1][jj][tid] : zero;
+            qk_item<ROPE, KV>(a, v, row, tt, hd, t0, q, qmask, wsm, cs[buf][tt], sn[buf][tt],
+                              ROPE ? 0.0f : scale_q[buf][tt], splat(tab.neg_zero));
         }
-    }
-    // Every copy issued was waited for above unless a wait gave up; then make sure none is still
-    // landing before the CTA leaves (bounded), and raise the fault word.
-    if (tid == 0 && fail) {
-        for (int bb = 0; bb < 2; ++bb)
-            if (uses[bb] > 0)
-                (void)mbar_wait(&full[bb], (uses[bb] - 1u) & 1u);
-        atomicOr(a.fault_word, kFaultCopyTimeout);
     }
 }
 
@@ -574,71 +536,31 @@ inline unsigned grid_for(int64_t units)
     return (unsigned)(units < (int64_t)(1 << 30) ? units : (int64_t)(1 << 30));
 }
 
-// Largest double buffer of the persistent Q/K kernel: 64 KB keeps 3 CTAs on an SM (2 tiles of
-// 2 tokens x 64 heads x 256 bytes for Beam's 48 + 8 heads with a KV cache).
-constexpr size_t kQkRingMaxSmem = 64 * 1024;
-
-// The persistent kernel with a KV cache: one quad per two items of a tile (256 threads for
-// 2 x 64 heads), as many CTAs as the double buffer lets the SMs hold.
-template <bool ROPE>
-cudaError_t launch_ring_qk(const QkArgs &a, const RopeTable &tab, int sms, int nheads,
-                           size_t smem, cudaStream_t stream)
-{
-    auto kern = qk_ring_kernel<ROPE, true>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess)
-        return e;
-    const int items = kRingTT * nheads;
-    int threads = 4 * ((items + 1) / 2);
-    threads = threads > kQkThreads ? kQkThreads : (threads + 31) / 32 * 32;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
-    if (e != cudaSuccess)
-        return e;
-    if (per_sm < 1)
-        return cudaErrorInvalidConfiguration;
-    const int64_t ntiles = (a.T + kRingTT - 1) / kRingTT;
-    const int64_t slots = (int64_t)sms * per_sm;
-    return launch_pdl(kern, dim3((unsigned)(ntiles < slots ? ntiles : slots)), dim3(threads),
-                      smem, stream, a, tab);
-}
-
 template <bool ROPE, bool KV>
-cudaError_t launch_qk(const QkArgs &a_in, cudaStream_t stream)
+cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
 {
     RopeTable tab;
     for (int i = 0; i < kHalf; ++i)
-        tab.inv_freq[i] = ROPE ? a_in.inv_freq_host[i] : 0.0f;
+        tab.inv_freq[i] = ROPE ? a.inv_freq_host[i] : 0.0f;
     tab.neg_zero = -0.0f;
-    QkArgs a = a_in;
-    a.fault_word = fault_word_device();
-    if (!a.fault_word)
-        return cudaErrorInvalidSymbol;
-    const int sms = device_sm_count();
-    const bool many = a.T >= 4 * (int64_t)sms;
-    cudaError_t e;
-    if constexpr (KV) {
-        // Many tokens with a KV cache: the persistent kernel, one tile ahead (it keeps the V
-        // rows' reads and the cache writes in flight beside the Q/K work).
-        const int nheads = a.n_q + 2 * a.n_kv;
-        const size_t smem = (size_t)2 * kRingTT * nheads * 256;
-        if (many && smem <= kQkRingMaxSmem) {
-            e = launch_ring_qk<ROPE>(a, tab, sms, nheads, smem, stream);
-            return e != cudaSuccess ? e : cudaGetLastError();
-        }
-    }
-    // Without the cache the direct kernel is the faster one: 4 CTAs of 8 warps on an SM, one
-    // head per quad per pass, and no barrier per tile.  Tiles of 8 tokens for RoPE (each thread
-    // then forms two cos/sin pairs per tile), 4 for SSMax: the faster of the sizes measured.
-    // Few tokens: one token per CTA spreads them over more SMs.
+    const bool many = a.T >= 4 * (int64_t)device_sm_count();
+    // Many tokens: 4 CTAs of 8 warps on an SM, one head per quad per pass, tiles of 8 tokens for
+    // RoPE (each thread then forms two cos/sin pairs per tile) and 4 for SSMax.  The staged
+    // kernel keeps a second pass's reads in flight; it pays off where a head costs the most
+    // arithmetic (RoPE) or the V rows add reads (the KV cache), while plain SSMax is as fast
+    // without it.  Few tokens: one token per CTA spreads them over more SMs.
     constexpr int TT = ROPE ? 8 : 4;
-    if (many)
-        e = launch_pdl(qk_norm_kernel<ROPE, TT, KV>, dim3(grid_for((a.T + TT - 1) / TT)),
-                       dim3(kQkThreads), 0, stream, a, tab);
-    else
-        e = launch_pdl(qk_norm_kernel<ROPE, 1, KV>, dim3(grid_for(a.T)), dim3(kQkThreads), 0,
-                       stream, a, tab);
+    const dim3 block(kQkThreads);
+    cudaError_t e;
+    if (many) {
+        const dim3 grid(grid_for((a.T + TT - 1) / TT));
+        if constexpr (ROPE || KV)
+            e = launch_pdl(qk_stage_kernel<ROPE, TT, KV>, grid, block, 0, stream, a, tab);
+        else
+            e = launch_pdl(qk_norm_kernel<ROPE, TT, KV>, grid, block, 0, stream, a, tab);
+    } else
+        e = launch_pdl(qk_norm_kernel<ROPE, 1, KV>, dim3(grid_for(a.T)), block, 0, stream, a,
+                       tab);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -75,7 +75,6 @@ struct QkArgs {
     float k_scale, v_scale;
     float k_inv, v_inv;     // 1 / scale, used only where the scale is a power of two
     bool k_pow2, v_pow2;
-    unsigned int *fault_word;  // the library's device fault word (set by the launcher)
 };
 
 struct RouteArgs {
@@ -116,9 +115,6 @@ cudaError_t launch_copy_timeout_selftest(unsigned long long limit_ns, cudaStream
 // The device fault word of the current device (bit 0: a kernel gave up waiting for its own bulk
 // copies); synchronous.
 cudaError_t read_fault_word(unsigned int *value, bool clear);
-
-// Device address of the fault word on the current device (cached per device).
-unsigned int *fault_word_device();
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

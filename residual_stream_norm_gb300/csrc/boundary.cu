@@ -872,24 +872,6 @@ cudaError_t launch_copy_timeout_selftest(unsigned long long limit_ns, cudaStream
     return cudaGetLastError();
 }
 
-unsigned int *fault_word_device()
-{
-    static std::mutex mu;
-    static int cached_dev = -1;
-    static unsigned int *cached_ptr = nullptr;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev != cached_dev) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess)
-            return nullptr;
-        cached_ptr = static_cast<unsigned int *>(p);
-        cached_dev = dev;
-    }
-    return cached_ptr;
-}
-
 int device_sm_count() { return device_sms(); }
 
 cudaError_t read_fault_word(unsigned int *value, bool clear)

@@ -60,9 +60,9 @@ def test_head_counts(kind, nq, nk):
 @pytest.mark.parametrize("T,nq,nk", [(609, 48, 8), (1999, 48, 8), (1001, 3, 2), (1001, 1, 0),
                                      (1001, 0, 1), (1001, 64, 8)])
 def test_many_tokens_ragged_tails(kind, T, nq, nk):
-    # From 4 x 152 tokens on, the persistent kernel: two-token tiles prefetched into shared
-    # memory a tile ahead, CTAs looping over several tiles, a one-token last tile for odd T.
-    # 64 + 8 heads do not fit its double buffer and take the direct kernel instead.
+    # From 4 x 152 tokens on, the multi-token tiles (8 tokens for RoPE, whose kernel stages the
+    # next pass in shared memory; 4 for SSMax), with ragged last tiles and passes, and head counts
+    # whose items do not fill a pass.
     c = bi.attn_qk_case(T=T, n_q=nq, n_kv=nk, seed=T + nq + nk)
     q = dev(c["q"]) if nq else torch.empty((T, 0, D), dtype=torch.bfloat16, device="cuda")
     k = dev(c["k"]) if nk else torch.empty((T, 0, D), dtype=torch.bfloat16, device="cuda")
