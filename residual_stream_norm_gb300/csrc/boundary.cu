@@ -46,6 +46,7 @@ __device__ unsigned int g_fault_word = 0u;
 namespace {
 
 constexpr int kMaxK = 16;
+constexpr int kRingMaxK = 8;  // the MoE ring holds K <= 8 routing coefficients in registers
 
 // Shared-memory slot of one warp in the rare exact path (beam_exact.cuh).
 struct ExactSlot {
@@ -327,8 +328,9 @@ __device__ __forceinline__ void combine_slot(f2 (&acc)[4], float ck, const unsig
         acc[j] = fma2(c2, widen(word(ev, j)), acc[j]);
 }
 
-template <bool SMEM>
-__device__ __forceinline__ uint4 combine_vec(const float (&c)[kMaxK], int K,
+// c holds KC >= K coefficients (the slots past K are zero).
+template <bool SMEM, int KC>
+__device__ __forceinline__ uint4 combine_vec(const float (&c)[KC], int K,
                                              const unsigned char *e0, size_t slot_bytes)
 {
     f2 acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -341,7 +343,7 @@ __device__ __forceinline__ uint4 combine_vec(const float (&c)[kMaxK], int K,
         for (int k = 0; k < K; ++k) {
             float ck = c[0];
 #pragma unroll
-            for (int kk = 1; kk < kMaxK; ++kk)  // register-resident select of c[k]
+            for (int kk = 1; kk < KC; ++kk)  // register-resident select of c[k]
                 ck = kk == k ? c[kk] : ck;
             combine_slot<SMEM>(acc, ck, e0 + (size_t)k * slot_bytes);
         }
@@ -358,11 +360,12 @@ __device__ __forceinline__ uint4 weight_vec(const void *w, int v, int nvec)
     return v < nvec ? ld_cached((const char *)w + 16 * (int64_t)v) : make_uint4(0u, 0u, 0u, 0u);
 }
 
+template <int KC>
 __device__ __forceinline__ void routing_coeffs(const BoundaryArgs &a, int64_t row,
-                                               float (&c)[kMaxK])
+                                               float (&c)[KC])
 {
 #pragma unroll
-    for (int k = 0; k < kMaxK; ++k)
+    for (int k = 0; k < KC; ++k)
         c[k] = k < a.K ? __fmul_rn(a.topk_w[row * a.K + k], a.routed_scaling) : 0.0f;
 }
 
@@ -523,7 +526,7 @@ __global__ void __launch_bounds__(NC + 32, MINB)
     }
     pdl_wait();
     const int lane = tid & 31;
-    float c[kMaxK], c_next[kMaxK];
+    float c[kRingMaxK], c_next[kRingMaxK];  // this row's and the next row's coefficients
     if constexpr (MOE) {
         if (my_rows > 0)
             routing_coeffs(a, first, c_next);
@@ -535,7 +538,7 @@ __global__ void __launch_bounds__(NC + 32, MINB)
         if constexpr (MOE) {
             // this row's coefficients were fetched during the previous row; fetch the next's
 #pragma unroll
-            for (int k = 0; k < kMaxK; ++k)
+            for (int k = 0; k < kRingMaxK; ++k)
                 c[k] = c_next[k];
             if (i + 1 < my_rows)
                 routing_coeffs(a, row + stride, c_next);
@@ -805,7 +808,7 @@ cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
     // prefetch kernel for the plain boundary and the warp-specialised TMA ring for the MoE
     // variant.
     const int chunks = (nvec + 127) / 128;
-    if (a.T >= 4 * (int64_t)sms && chunks <= 8) {
+    if (a.T >= 4 * (int64_t)sms && chunks <= 8 && (!MOE || a.K <= kRingMaxK)) {
         if constexpr (MOE)
             return launch_ring_chunks<kMoeConsumers, true, kMoeCtasPerSm>(a, chunks, sms, stream);
         else
