@@ -194,13 +194,24 @@ __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], ch
     if constexpr (ROPE) {
         // The rotation can cancel, so an FP32 ulp of r could move an output by more than a BF16
         // ulp: the head sum is rounded as the exact sum would be.
-        Sum2x2 acc = {0ull, 0ull};
+        // Each of the two packed accumulators starts from M, the largest square of the lane,
+        // so that its running sum is never below the next term and Dekker's Fast2Sum (3 adds)
+        // is exact in place of TwoSum (6); 2M is taken off after the lanes are merged.
+        float mabs = 0.0f;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp)
-                sum2_add(acc, mul2(x[jj][pp], x[jj][pp]));
+                mabs = fmaxf(mabs, fmaxf(fabsf(lo_of(x[jj][pp])), fabsf(hi_of(x[jj][pp]))));
+        const float m2 = __fmul_rn(mabs, mabs);  // exact: the square of a BF16 value
+        Sum2x2 acc = {splat(m2), 0ull};
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int pp = 0; pp < 4; ++pp)
+                fast2_add(acc, mul2(x[jj][pp], x[jj][pp]));
         Sum2 tot = sum_merge(Sum2{lo_of(acc.hi), lo_of(acc.lo)}, Sum2{hi_of(acc.hi), hi_of(acc.lo)});
+        tot = sum_merge(tot, Sum2{-__fadd_rn(m2, m2), 0.0f});
 #pragma unroll
         for (int off = 1; off < 4; off <<= 1) {
             Sum2 o;
@@ -209,7 +220,9 @@ __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], ch
             tot = sum_merge(tot, o);
         }
         ms = sum_value(tot);
-        const bool tie = near_tie(tot.hi, tot.lo, ms);  // the same in the quad
+        // the same in the quad; a non-finite sum (an infinite or NaN square, or a seeded sum
+        // past the FP32 range) is decided by the exact path too
+        const bool tie = near_tie(tot.hi, tot.lo, ms) || !isfinite(ms);
         if constexpr (KV) {
             if (tie)  // rare
                 ms = head_sum_exact(row, q, qmask);

@@ -153,7 +153,10 @@ __device__ __forceinline__ Sum2 warp_sum(Sum2 a, int width = 32)
 // The compensated sums above are within 2^-37 relative of the exact sum of their (non-negative,
 // exactly computed) terms: an accumulator of m terms errs by at most m^2/2 u^2 (u = 2^-24; a
 // thread splits its n <= 64 terms over two accumulators, n^2/4 u^2 <= 2^-38) and each of at most
-// ten merge levels by about 5 u^2 more.  RN(hi + lo) is the FP32 rounding of the exact sum unless
+// ten merge levels by about 5 u^2 more.  An accumulator seeded with an upper bound M <= S of its
+// terms (S the sum of all the thread's terms; Fast2Sum in place of TwoSum, M taken off afterwards
+// by an exact TwoSum) keeps its running sum below 2S, so its m error terms add up with an error
+// of at most 2 m^2 u^2 S: 2^-39 S for the 16 terms of each of a RoPE lane's two accumulators.  RN(hi + lo) is the FP32 rounding of the exact sum unless
 // hi + lo lies within that distance of a rounding boundary; near_tie() detects those sums
 // (about 2^-12 of them) so that they can be recomputed exactly in integer arithmetic
 // (beam_exact.cuh).

@@ -167,6 +167,16 @@ __device__ __forceinline__ void sum2_add(Sum2x2 &a, f2 t)
     a.lo = add2(a.lo, e);
 }
 
+// Adds t >= 0 to an accumulator whose running sum is at least t (both lanes): Dekker's Fast2Sum,
+// exact under that condition.
+__device__ __forceinline__ void fast2_add(Sum2x2 &a, f2 t)
+{
+    const f2 s = add2(a.hi, t);
+    const f2 e = sub2(t, sub2(s, a.hi));
+    a.hi = s;
+    a.lo = add2(a.lo, e);
+}
+
 // Merge of two packed accumulators (TwoSum of the hi parts, error added to the lo parts).
 __device__ __forceinline__ Sum2x2 sum2_merge(const Sum2x2 &a, const Sum2x2 &b)
 {

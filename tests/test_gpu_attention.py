@@ -105,6 +105,36 @@ def test_rope_theta_and_special_positions():
         assert_bf16_close(u16(k), wk, what=f"rope theta={theta}")
 
 
+@pytest.mark.parametrize("kind", ["rope", "ssmax"])
+@pytest.mark.parametrize("T", [5, 1001])
+def test_extreme_and_nonfinite_heads(kind, T):
+    # Heads whose sum of squares sits near the top of the FP32 range, overflows, is NaN, is zero
+    # or underflows; every other head random.  The kernels must give the oracle's IEEE results.
+    c = bi.attn_qk_case(T=T, seed=61)
+    q = u16(c["q"]).copy()
+    def bits(v):  # BF16 bits of a value
+        return int(oracle.bf16_rne(np.array([v], np.float32))[0])
+
+    big = bits(1.3e19)                                # square 1.69e38: two of them stay finite
+    for t in range(T):
+        h = q[t]
+        h[0, :] = 0
+        h[0, 0] = h[0, 1] = big                       # one lane holds both large squares
+        h[1, :] = 0
+        h[1, 5] = bits(2e19)                          # its square overflows: the sum is inf
+        h[2, 7] = 0x7FC0                              # NaN
+        h[3, 9] = 0x7F80                              # +inf
+        h[4, :] = 0                                   # all zero
+        h[5, :] = bits(2.0 ** -70)                    # squares underflow
+        h[6, 64] = big                                # partners of a large element
+        h[6, 0] = bits(-1.3e19)
+    c["q"] = bi.from_u16(q)
+    qo, ko = run_qk(kind, c)
+    wq, wk = oracle_qk(kind, c)
+    assert_bf16_close(u16(qo), wq, what=f"{kind} extreme q T={T}")
+    assert_bf16_close(u16(ko), wk, what=f"{kind} extreme k T={T}")
+
+
 def test_ssmax_parameters_and_positions():
     c = bi.attn_qk_case(T=6, seed=24)
     c["pos"] = torch.tensor([0, 63487, 2095103, 7, 1 << 20, 123456], dtype=torch.int64)
