@@ -167,8 +167,10 @@ def test_zero_tokens_is_a_no_op():
     assert bool((out.view == -12345.0).all())
 
 
-def test_nonfinite_and_degenerate_rows():
-    c = bi.boundary_case(T=8, n=4, seed=11)
+@pytest.mark.parametrize("T", [8, 700])
+def test_nonfinite_and_degenerate_rows(T):
+    # the first 8 rows degenerate (T = 700: the prefetch kernel), the rest random
+    c = bi.boundary_case(T=T, n=4, seed=11)
     x = u16(c["x"]).copy()
     h = u16(c["h"]).copy()
     x[0, 17] = 0x7FC0          # NaN
@@ -178,6 +180,8 @@ def test_nonfinite_and_degenerate_rows():
     h[4, 100] = 0xFF80         # -inf in the residual
     x[5, :] = 0x7F7F           # largest finite: squares overflow FP32
     x[6, ::2] = 0x0080         # smallest normals
+    x[7, :] = 0                # two squares of 1.69e38 in one thread: the row sum 3.38e38 is
+    x[7, :2] = 0x5F34          # finite, though a partial sum seeded with the largest square is not
     hh, xx = bi.from_u16(h), bi.from_u16(x)
     got = run_gpu(hh, xx, c["w_post"], c["w_pre"], 4)
     want = oracle.boundary(h, x, u16(c["w_post"]), u16(c["w_pre"]), 4)
