@@ -815,8 +815,11 @@ cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
             return launch_pf(a, chunks, sms, stream);
     }
     // Few rows (or very wide rows): one CTA per row straight from memory.
+    // Blocks of at most 512 threads for few rows (320 for H = 5120, two vectors a thread: a
+    // decode boundary took 2.74 us in a CUDA graph, against 3.13 us with 640 threads of one
+    // vector and 3.22 us with 160 of four), 256 or 320 otherwise.
     const bool small = a.T < 2 * (int64_t)sms;
-    const int max_threads = small ? 1024 : (MOE ? 320 : 256);
+    const int max_threads = small ? 512 : (MOE ? 320 : 256);
     const int vpt = pick_vpt(nvec, max_threads);
     const int threads = round_warps((nvec + vpt - 1) / vpt);
     const dim3 grid((unsigned)(a.T < (int64_t)(1 << 30) ? a.T : (int64_t)(1 << 30)));
