@@ -358,6 +358,26 @@ def copy_ceiling(device, nbytes: int = 1 << 30, reps: int = 20) -> dict:
             "how": "torch copy_ of a 1 GiB device buffer (read + write), 20 reps, CUDA events"}
 
 
+def host_link(device, nbytes: int = 1 << 28, reps: int = 5) -> dict:
+    """Pinned host <-> device copy bandwidth measured in this run (one direction at a time), the
+    ceiling of the end-to-end number."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    out = {}
+    for name, (dst, src) in (("h2d_gb_s", (d, h)), ("d2h_gb_s", (h, d))):
+        dst.copy_(src, non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(device)
+        e0.record()
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize(device)
+        out[name] = round(nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    del h, d
+    return out
+
+
 def decode_chain_us(device, replays: int = 200) -> dict:
     """Batch-1 decode: 104 boundary launches n = 1..104 captured in one CUDA graph."""
     import residual_stream_norm_gb300 as rsn
@@ -559,9 +579,13 @@ def run_gpu_arm(args) -> None:
     e2e = {"value": round(ws * T * e2e_steps / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
            "path": "pinned host buffers -> cudaMemcpyAsync -> C ABI -> cudaMemcpyAsync -> host; "
-                   "copy-in, compute and copy-out streams pipelined over two buffer sets (the "
-                   "host link, about 270 GB/s both ways together here, bounds it)"}
+                   "copy-in, compute and copy-out streams pipelined over two buffer sets; the "
+                   "host link bounds it (host_link: each direction's copy bandwidth measured "
+                   "in this run, and the bytes/s the pipelined run moved both ways)"}
     del sets[1]
+    e2e["host_link"] = host_link(device)
+    # bytes that cross the host link per second of the pipelined run, both ways together
+    e2e["host_link"]["e2e_gb_s"] = round((h2d + d2h) * e2e_steps / (e2e_ms * 1e-3) / 1e9, 1)
 
     decode = decode_chain_us(device)
     nxt = next_rows(host, device, peak)
