@@ -424,8 +424,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
 // A CTA has NC consumer threads (a multiple of 32) and one producer warp.  Its rows are
 // blockIdx.x, blockIdx.x + gridDim.x, ...; each row is cut into VPT chunks of NC 16-byte
 // vectors, and consumer thread t owns vector c * NC + t of chunk c.  A unit of work is one chunk
-// of one row; its stage holds KIN input slices (the x chunk, or the K expert chunks) and the h
-// chunk, each NC * 16 bytes.  Per stage two mbarriers: `full` completes when the producer's
+// of one row; its stage holds the K expert chunks and the h chunk, each NC * 16 bytes.  Per stage two mbarriers: `full` completes when the producer's
 // bulk copies have landed (transaction bytes), `empty` when all consumer warps have read the
 // stage (one arrive per warp).  The producer keeps `stages` units in flight.
 
@@ -437,9 +436,9 @@ constexpr int kRingMaxStages = 16;
 constexpr int kMoeConsumers = 128;
 constexpr int kMoeCtasPerSm = 3;
 
-template <int NC, int VPT, bool MOE, int MINB>
+template <int NC, int VPT, int MINB>
 __global__ void __launch_bounds__(NC + 32, MINB)
-    boundary_ring_kernel(const BoundaryArgs a, int stages)
+    moe_ring_kernel(const BoundaryArgs a, int stages)
 {
     extern __shared__ __align__(128) unsigned char dyn[];
     uint64_t *full = reinterpret_cast<uint64_t *>(dyn);
@@ -453,7 +452,7 @@ __global__ void __launch_bounds__(NC + 32, MINB)
     constexpr uint32_t kSlice = NC * 16;
     const int nvec = a.H >> 3;
     const int tid = threadIdx.x;
-    const int KIN = MOE ? a.K : 1;
+    const int KIN = a.K;
     const uint32_t stage_bytes = (uint32_t)(KIN + 1) * kSlice;
     // the consumer threads park their slices of w_post and w_pre here ([2][VPT][NC] vectors):
     // read from shared memory inside the chain, they cost no long-latency loads
@@ -494,8 +493,8 @@ __global__ void __launch_bounds__(NC + 32, MINB)
             const size_t col = (size_t)c * kSlice;
             mbar_arrive_expect_tx(&full[st], (uint32_t)(KIN + 1) * bytes);
             for (int k = 0; k < KIN; ++k) {
-                const char *src = MOE ? (const char *)a.expert_out + ((size_t)row * KIN + k) * 2 * a.H
-                                      : (const char *)a.x_in + (size_t)row * 2 * a.H;
+                const char *src =
+                    (const char *)a.expert_out + ((size_t)row * KIN + k) * 2 * a.H;
                 bulk_g2s(dst + (size_t)k * kSlice, src + col, bytes, &full[st]);
             }
             bulk_g2s(dst + (size_t)KIN * kSlice, (const char *)a.h_in + (size_t)row * 2 * a.H + col,
@@ -527,22 +526,18 @@ __global__ void __launch_bounds__(NC + 32, MINB)
     pdl_wait();
     const int lane = tid & 31;
     float c[kRingMaxK], c_next[kRingMaxK];  // this row's and the next row's coefficients
-    if constexpr (MOE) {
-        if (my_rows > 0)
-            routing_coeffs(a, first, c_next);
-    }
+    if (my_rows > 0)
+        routing_coeffs(a, first, c_next);
     int st = 0;          // stage of the next unit
     uint32_t parity = 0;  // phase parity of that stage's `full` barrier for this pass
     for (int64_t i = 0; i < my_rows; ++i) {
         const int64_t row = first + i * stride;
-        if constexpr (MOE) {
-            // this row's coefficients were fetched during the previous row; fetch the next's
+        // this row's coefficients were fetched during the previous row; fetch the next's
 #pragma unroll
-            for (int k = 0; k < kRingMaxK; ++k)
-                c[k] = c_next[k];
-            if (i + 1 < my_rows)
-                routing_coeffs(a, row + stride, c_next);
-        }
+        for (int k = 0; k < kRingMaxK; ++k)
+            c[k] = c_next[k];
+        if (i + 1 < my_rows)
+            routing_coeffs(a, row + stride, c_next);
         uint4 xv[VPT], hv[VPT];
 #pragma unroll
         for (int ch = 0; ch < VPT; ++ch) {
@@ -550,10 +545,7 @@ __global__ void __launch_bounds__(NC + 32, MINB)
             const unsigned char *stage = ring + (size_t)st * stage_bytes;
             if (ch * NC + tid < nvec) {
                 hv[ch] = *reinterpret_cast<const uint4 *>(stage + (size_t)KIN * kSlice + 16 * tid);
-                if constexpr (MOE)
-                    xv[ch] = combine_vec<true>(c, KIN, stage + 16 * tid, kSlice);
-                else
-                    xv[ch] = *reinterpret_cast<const uint4 *>(stage + 16 * tid);
+                xv[ch] = combine_vec<true>(c, KIN, stage + 16 * tid, kSlice);
             } else {
                 xv[ch] = make_uint4(0u, 0u, 0u, 0u);
                 hv[ch] = xv[ch];
@@ -691,11 +683,11 @@ int device_sms()
     return cached_sms;
 }
 
-template <int NC, int VPT, bool MOE, int MINB>
+template <int NC, int VPT, int MINB>
 cudaError_t launch_ring(const BoundaryArgs &a, int stages, size_t smem, int sms,
                         cudaStream_t stream)
 {
-    auto kern = boundary_ring_kernel<NC, VPT, MOE, MINB>;
+    auto kern = moe_ring_kernel<NC, VPT, MINB>;
     const int threads = NC + 32;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -729,30 +721,24 @@ int pick_vpt(int nvec, int max_threads)
 
 inline int round_warps(int n) { return (n + 31) / 32 * 32; }
 
-// The ring launch for rows of `chunks` chunks of NC vectors.  Stages: as many as fit beside the
-// parked weights in this CTA's share of the SM's 228 KB of shared memory (less 3 KB for the
-// static arrays and the per-CTA reserve), between 2 and 16; 2 for the MoE variant, whose
-// stages hold K + 1 slices.
-template <int NC, bool MOE, int MINB>
+// The MoE ring launch for rows of `chunks` chunks of NC vectors: 2 stages of K + 1 slices beside
+// the parked weights.
+template <int NC, int MINB>
 cudaError_t launch_ring_chunks(const BoundaryArgs &a, int chunks, int sms, cudaStream_t stream)
 {
-    const size_t stage = (size_t)((MOE ? a.K : 1) + 1) * NC * 16;
+    const int stages = 2;
+    const size_t stage = (size_t)(a.K + 1) * NC * 16;
     const size_t weights = (size_t)2 * chunks * NC * 16;
-    const size_t budget = (size_t)228 * 1024 / MINB - 3 * 1024;
-    int stages = MOE ? 2
-                     : (int)((budget > weights + kRingHeader ? budget - weights - kRingHeader : 0) /
-                             stage);
-    stages = stages < 2 ? 2 : (stages > kRingMaxStages ? kRingMaxStages : stages);
     const size_t smem = kRingHeader + stages * stage + weights;
     switch (chunks) {
-    case 1: return launch_ring<NC, 1, MOE, MINB>(a, stages, smem, sms, stream);
-    case 2: return launch_ring<NC, 2, MOE, MINB>(a, stages, smem, sms, stream);
-    case 3: return launch_ring<NC, 3, MOE, MINB>(a, stages, smem, sms, stream);
-    case 4: return launch_ring<NC, 4, MOE, MINB>(a, stages, smem, sms, stream);
-    case 5: return launch_ring<NC, 5, MOE, MINB>(a, stages, smem, sms, stream);
-    case 6: return launch_ring<NC, 6, MOE, MINB>(a, stages, smem, sms, stream);
-    case 7: return launch_ring<NC, 7, MOE, MINB>(a, stages, smem, sms, stream);
-    default: return launch_ring<NC, 8, MOE, MINB>(a, stages, smem, sms, stream);
+    case 1: return launch_ring<NC, 1, MINB>(a, stages, smem, sms, stream);
+    case 2: return launch_ring<NC, 2, MINB>(a, stages, smem, sms, stream);
+    case 3: return launch_ring<NC, 3, MINB>(a, stages, smem, sms, stream);
+    case 4: return launch_ring<NC, 4, MINB>(a, stages, smem, sms, stream);
+    case 5: return launch_ring<NC, 5, MINB>(a, stages, smem, sms, stream);
+    case 6: return launch_ring<NC, 6, MINB>(a, stages, smem, sms, stream);
+    case 7: return launch_ring<NC, 7, MINB>(a, stages, smem, sms, stream);
+    default: return launch_ring<NC, 8, MINB>(a, stages, smem, sms, stream);
     }
 }
 
@@ -810,7 +796,7 @@ cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
     const int chunks = (nvec + 127) / 128;
     if (a.T >= 4 * (int64_t)sms && chunks <= 8 && (!MOE || a.K <= kRingMaxK)) {
         if constexpr (MOE)
-            return launch_ring_chunks<kMoeConsumers, true, kMoeCtasPerSm>(a, chunks, sms, stream);
+            return launch_ring_chunks<kMoeConsumers, kMoeCtasPerSm>(a, chunks, sms, stream);
         else
             return launch_pf(a, chunks, sms, stream);
     }
