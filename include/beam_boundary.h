@@ -70,9 +70,10 @@ BEAM_API const char *beam_status_str(int status);
  * Returns BEAM_ERR_INVALID_ARG for n < 1 or NULL outputs. */
 BEAM_API int beam_residual_scales(int32_t n, float *alpha, float *s);
 
-/* Fault word of the current device.  The persistent kernels wait on their own bulk copies with a
- * time limit (2 s); a kernel that gives up drains its copies, sets bit 0 (1 = copy wait timed
- * out) and returns without writing the rest of its rows.  Never set in normal operation.
+/* Fault word of the current device.  The persistent boundary kernels (the many-row plain and MoE
+ * boundaries) wait on their own bulk copies with a time limit (2 s); a kernel that gives up
+ * drains its copies, sets bit 0 (1 = copy wait timed out) and returns without writing valid
+ * rows.  Never set in normal operation.
  * Synchronous (a device-to-host copy on the legacy default stream); `clear` != 0 resets the word.
  * No counterpart on the pages: a diagnostic of this library. */
 BEAM_API int beam_device_faults(uint32_t *flags, int clear);
@@ -80,7 +81,7 @@ BEAM_API int beam_device_faults(uint32_t *flags, int clear);
 /* Diagnostic: exercises the copy-timeout path of the persistent kernels without a fault.  One
  * CTA arms an mbarrier for 16 bytes that no copy delivers, waits with the kernels' bounded wait
  * for limit_ns nanoseconds (1 us .. 2 s), gives up and sets bit 0 of the device fault word, as a
- * ring kernel whose copies stalled would; nothing is left in flight.  Asynchronous on `stream`;
+ * persistent kernel whose copies stalled would; nothing is left in flight.  Asynchronous on `stream`;
  * read the result with beam_device_faults().  BEAM_ERR_INVALID_ARG for a limit out of range. */
 BEAM_API int beam_selftest_copy_timeout(int64_t limit_ns, cudaStream_t stream);
 
