@@ -217,8 +217,9 @@ __device__ __forceinline__ bool route_token(const float (&s)[kPerLane],
     return all_finite && cm < 1.0e30f && __fsub_rn(g4, g5) > 2.0f * dg && mingap > 2.0f * dc;
 }
 
-// 3 CTAs per SM: more warps to cover the ranking's dependent-instruction latency, at 80
-// registers (its spills sit in the rare exact-sigmoid path); 49.4 -> 46.4 us at T = 16384.
+// 3 CTAs per SM: more warps to cover the ranking's dependent-instruction latency.  At the 80
+// registers this allows the kernel spills a little, and is still faster than at 2 CTAs and 124
+// registers without spills (46.4 against 49.4 us at T = 16384; 4 CTAs gave 46.5).
 __global__ void __launch_bounds__(kRouteThreads, 3)
     grouped_topk_kernel(const RouteArgs a)
 {
