@@ -427,7 +427,7 @@ def next_rows(host: dict, device, peak: float, iters: int = 50) -> dict:
     """Rows beyond the five-kernel step at the step's T, each launch timed alone with CUDA
     events: the Q/K kernels fused with an FP8 KV-cache write (inputs larger than L2), and the
     grouped routing (16.8 MB of logits: L2-resident between launches, so its GB/s is not an
-    HBM figure; it is bound by its correctly rounded sigmoids)."""
+    HBM figure; it is bound by the integer ALU work of its ranking)."""
     import residual_stream_norm_gb300 as rsn
     T = host["q_r"].shape[0]
     kv = bi.kv_cache_case(T=T, pad_frac=0.0, oob_frac=0.0, seed=7)
@@ -472,8 +472,11 @@ def next_rows(host: dict, device, peak: float, iters: int = 50) -> dict:
             out[name]["cache"] = (f"FP8 E4M3, {kv['num_slots']} slots, one distinct random "
                                   "slot per token")
         else:
-            out[name]["note"] = ("256 experts, 8 groups, top-4 groups, top-8; bound by the "
-                                 "correctly rounded FP32 sigmoids, not by HBM")
+            out[name]["bound"] = "alu"
+            out[name]["note"] = ("256 experts, 8 groups, top-4 groups, top-8; bound by the SM's "
+                                 "integer ALU pipe (the ranking's compares and selects: 78% busy "
+                                 "while the SMs are active, in the committed ncu capture), not "
+                                 "by HBM; its GB/s fraction is not a roofline")
     return out
 
 
