@@ -65,7 +65,9 @@ def test_decode_moe_boundaries_layers_3_to_51():
                                    # persistent TMA ring (>= 4 rows per SM), and shapes whose
                                    # stages do not fit shared memory (per-row fallback)
                                    (700, 5120, 8), (650, 5128, 1), (620, 16384, 2),
-                                   (610, 5120, 16), (900, 16384, 8), (1500, 8, 8)])
+                                   (610, 5120, 16), (900, 16384, 8), (1500, 8, 8),
+                                   # the 3-stage ring with fewer slots and other row widths
+                                   (700, 1032, 3), (640, 4096, 8), (999, 6144, 7)])
 def test_shapes(T, H, K):
     c = bi.moe_case(T=T, H=H, K=K, seed=T * 7 + K)
     check(run_gpu(c["h"], c["e"], c["topk_w"], c["w_post"], c["w_pre"], c["n"]), oracle_run(c),
