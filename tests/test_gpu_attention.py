@@ -135,6 +135,24 @@ def test_extreme_and_nonfinite_heads(kind, T):
     assert_bf16_close(u16(ko), wk, what=f"{kind} extreme k T={T}")
 
 
+@pytest.mark.parametrize("kind", ["rope", "ssmax"])
+@pytest.mark.parametrize("T", [5, 1001])
+@pytest.mark.parametrize("eps", [0.0, 1e-2])
+def test_eps_zero_and_large(kind, T, eps):
+    # eps = 0: an all-zero head has r = 1/sqrt(0) = inf and NaN outputs, as in the oracle;
+    # eps = 1e-2: the norm of small heads is dominated by eps
+    c = bi.attn_qk_case(T=T, seed=71)
+    q = u16(c["q"]).copy()
+    q[:, 0, :] = 0
+    small = (q[:, 1, :].astype(np.uint32) << 16).view(np.float32) * np.float32(2.0 ** -10)
+    q[:, 1, :] = oracle.bf16_rne(small)
+    c["q"] = bi.from_u16(q)
+    qo, ko = run_qk(kind, c, eps=eps)
+    wq, wk = oracle_qk(kind, c, eps=eps)
+    assert_bf16_close(u16(qo), wq, what=f"{kind} eps={eps} q T={T}")
+    assert_bf16_close(u16(ko), wk, what=f"{kind} eps={eps} k T={T}")
+
+
 def test_ssmax_parameters_and_positions():
     c = bi.attn_qk_case(T=6, seed=24)
     c["pos"] = torch.tensor([0, 63487, 2095103, 7, 1 << 20, 123456], dtype=torch.int64)

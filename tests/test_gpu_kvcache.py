@@ -97,11 +97,14 @@ def test_qk_kv_configs(kind, fp8, T, mode):
 
 @pytest.mark.parametrize("kind", ["rope", "ssmax"])
 @pytest.mark.parametrize("k_scale,v_scale", [(0.5, 4.0), (3.0, 0.3)])
-def test_fp8_scales_power_of_two_and_general(kind, k_scale, v_scale):
-    c = bi.attn_qk_case(T=64, seed=5)
-    kv = bi.kv_cache_case(T=64, seed=6)
+@pytest.mark.parametrize("T", [64, 1001])
+def test_fp8_scales_power_of_two_and_general(kind, k_scale, v_scale, T):
+    # T = 1001: the staged kernel, with a ragged last tile
+    c = bi.attn_qk_case(T=T, seed=5)
+    kv = bi.kv_cache_case(T=T, seed=6)
     got = run(kind, c, kv, True, k_scale, v_scale)
-    check_caches(kind, c, kv, True, got, k_scale, v_scale, what=f"scales {k_scale},{v_scale}")
+    check_caches(kind, c, kv, True, got, k_scale, v_scale,
+                 what=f"scales {k_scale},{v_scale} T={T}")
 
 
 @pytest.mark.parametrize("T", [9, 1001])
