@@ -199,3 +199,24 @@ def prefill_boundary_case(T: int = 16384, H: int = HIDDEN, seed: int = 0) -> dic
     w_post = torch.stack([norm_weight(g, H) for _ in range(N_BOUNDARIES)])
     w_pre = torch.stack([norm_weight(g, H) for _ in range(N_BOUNDARIES)])
     return dict(h=h, x=x, w_post=w_post, w_pre=w_pre, eps=EPS)
+
+
+TP_RANKS = 8
+
+
+def allreduce_case(T: int = 128, H: int = HIDDEN, P: int = TP_RANKS, n: int = 7, seed: int = 0,
+                   outlier_frac: float = 0.01, outlier_mult: float = 16.0) -> dict:
+    """Tensor-parallel sublayer output over P ranks: partials x_p [P, T, H], each
+    N(0, 1) * s_t / sqrt(P) with one s_t ~ U(0.5, 4) per token shared by the ranks (so the sum
+    has the prefill case's spread), a fraction of the tokens x``outlier_mult`` on every rank;
+    h ~ N(0, 1); norm weights 1 + 0.1 N(0, 1); residual index n."""
+    g = rng(seed)
+    s_t = g.uniform(0.5, 4.0, size=T).astype(np.float32) / np.float32(np.sqrt(P))
+    if outlier_frac > 0 and T > 0:
+        idx = g.choice(T, size=max(1, int(round(outlier_frac * T))), replace=False)
+        s_t[idx] *= np.float32(outlier_mult)
+    parts = normal(g, (P, T, H))
+    parts *= s_t[None, :, None]
+    h = to_bf16(normal(g, (T, H)))
+    return dict(h=h, parts=to_bf16(parts), w_post=norm_weight(g, H), w_pre=norm_weight(g, H),
+                n=n, eps=EPS)

@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
             so.orc_moe_combine_boundary.argtypes = [u16p, u16p, u16p, u16p, f32p, f32, u16p,
                                                     u16p, i64, i32, i32, i32, f32, f32p, u16p,
                                                     f32p]
+            so.orc_allreduce_boundary.argtypes = [u16p, u16p, u16p, u16p, i32, u16p, u16p, i64,
+                                                  i32, i32, f32, f32p, u16p, f32p]
             so.orc_qk_norm_rope.argtypes = [u16p, u16p, i64, i64, u16p, u16p, i64p, i64, i32,
                                             i32, i32, f32, f32, f32p]
             so.orc_qk_norm_ssmax.argtypes = [u16p, u16p, i64, i64, u16p, u16p, i64p, i64, i32,
@@ -88,7 +90,8 @@ def lib() -> ctypes.CDLL:
             so.orc_kv_cache_write.argtypes = [ctypes.c_void_p, ctypes.c_void_p, u16p, u16p, i64,
                                               i64, i64p, i64, i32, i32, i64, i32, f32, f32]
             for fn in ("orc_bf16_rne_array", "orc_residual_scales", "orc_rope_inv_freq",
-                       "orc_boundary", "orc_moe_combine_boundary", "orc_qk_norm_rope",
+                       "orc_boundary", "orc_moe_combine_boundary", "orc_allreduce_boundary",
+                       "orc_qk_norm_rope",
                        "orc_qk_norm_ssmax", "orc_attn_gate", "orc_kv_cache_write"):
                 getattr(so, fn).restype = None
             _lib = so
@@ -193,6 +196,30 @@ def moe_combine_boundary(h, expert_out, topk_w, w_post, w_pre, n: int, eps: floa
     lib().orc_moe_combine_boundary(_ptr(h_out, u), _ptr(y, u), _ptr(h, u), _ptr(e, u),
                                    _ptr(w, f), routed_scaling, _ptr(w_post, u), _ptr(w_pre, u),
                                    T, H, K, n, eps, _ptr(rstd, f), _ptr(x_out, u), _ptr(work, f))
+    return (h_out, y, rstd, x_out) if return_x else (h_out, y, rstd)
+
+
+def allreduce_boundary(h, parts, w_post, w_pre, n: int, eps: float = 1e-6,
+                       return_x: bool = False):
+    """Tensor-parallel partial outputs summed in rank order in FP32 and rounded once to BF16,
+    then the boundary chain.
+
+    h: [T, H] uint16; parts: [P, T, H] uint16 (rank p's partial sublayer output at parts[p]).
+    Returns (h_out, y, rstd[T, 2]) or (h_out, y, rstd, x) with ``return_x``."""
+    h, w_post, w_pre = _u16(h), _u16(w_post), _u16(w_pre)
+    parts = _u16(parts)
+    P, T, H = parts.shape
+    assert h.shape == (T, H) and w_post.shape == (H,) and w_pre.shape == (H,)
+    assert P >= 1 and n >= 1
+    h_out = np.empty_like(h)
+    y = np.empty_like(h)
+    rstd = np.empty((T, 2), dtype=np.float32)
+    x_out = np.empty_like(h) if return_x else None
+    work = np.empty(3 * H, dtype=np.float32)
+    u, f = ctypes.c_uint16, ctypes.c_float
+    lib().orc_allreduce_boundary(_ptr(h_out, u), _ptr(y, u), _ptr(h, u), _ptr(parts, u), P,
+                                 _ptr(w_post, u), _ptr(w_pre, u), T, H, n, eps, _ptr(rstd, f),
+                                 _ptr(x_out, u), _ptr(work, f))
     return (h_out, y, rstd, x_out) if return_x else (h_out, y, rstd)
 
 

@@ -283,6 +283,43 @@ void orc_moe_combine_boundary(uint16_t *h_out, uint16_t *y_out, const uint16_t *
 }
 
 /* ------------------------------------------------------------------------------------------ */
+/* Tensor-parallel all-reduce of the sublayer output fused ahead of the boundary               */
+/* ------------------------------------------------------------------------------------------ */
+
+/* Under tensor parallelism over P ranks each rank holds a partial sublayer output x_p (BF16);
+ * the sublayer output is their sum.  Per element, in rank order:
+ *   s_0 = x_{0,j};   s_p = fp32(s_{p-1} + x_{p,j}) for p = 1..P-1;   x_j = bf16(s_{P-1})
+ * (FP32 adds, one BF16 rounding), then the boundary chain on x.  With P = 1 this is the plain
+ * boundary on x_0.
+ * [vLLM] "Agentengetriebene Optimierung", change 3 (both TP all-reduces of a layer run inside
+ * the norm kernel); [SGL] kernel-fusion paragraph (all-reduce, output norm, scaled residual add
+ * and the next layer's input norm fused).  Neither page states the accumulation order; rank
+ * order in FP32 is the plainest reading of "FP32 math" ([vLLM] change 1).
+ * parts: [P, T, H] BF16 (rank p's partial at parts + p*T*H); x_out: [T, H] or NULL. */
+void orc_allreduce_boundary(uint16_t *h_out, uint16_t *y_out, const uint16_t *h_in,
+                            const uint16_t *parts, int32_t P, const uint16_t *w_post,
+                            const uint16_t *w_pre, int64_t T, int32_t H, int32_t n, float eps,
+                            float *rstd_out, uint16_t *x_out, float *work)
+{
+    float alpha, s;
+    orc_residual_scales(n, &alpha, &s);
+    float *xf = work + 2 * (int64_t)H;
+    const int64_t plane = T * (int64_t)H;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int32_t j = 0; j < H; ++j) {
+            float acc = orc_bf16_to_f32(parts[t * H + j]);
+            for (int32_t p = 1; p < P; ++p)
+                acc = acc + orc_bf16_to_f32(parts[p * plane + t * H + j]);
+            xf[j] = bf16_round(acc);
+            if (x_out)
+                x_out[t * H + j] = orc_bf16_rne(acc);
+        }
+        boundary_token(h_out + t * H, y_out + t * H, h_in + t * H, xf, w_post, w_pre, H, alpha,
+                       s, eps, rstd_out ? rstd_out + 2 * t : 0, work);
+    }
+}
+
+/* ------------------------------------------------------------------------------------------ */
 /* Per-head Q/K RMSNorm fused with RoPE (sliding-window layers) or SSMax (NoPE layers)          */
 /* ------------------------------------------------------------------------------------------ */
 
