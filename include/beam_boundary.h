@@ -12,7 +12,8 @@
  * --------------------------------
  *  - BF16 tensors are passed as `void*` to IEEE bfloat16 storage; FP32 tensors as `float*`.
  *  - Every pointer is a device pointer on the CURRENT CUDA device.  The caller allocates, owns
- *    and frees every buffer; the library never allocates, frees or synchronises.
+ *    and frees every buffer; the library never allocates or frees memory, and no call
+ *    synchronises except the beam_device_faults diagnostic.
  *  - Every call is asynchronous on `stream` (0 = the legacy default stream).  The returned status
  *    reflects the argument checks and `cudaGetLastError()` right after the launch; a fault that
  *    happens later surfaces on the next synchronising CUDA call, as for any kernel.
@@ -41,7 +42,7 @@
 extern "C" {
 #endif
 
-#define BEAM_ABI_VERSION 1
+#define BEAM_ABI_VERSION 2
 
 /* Symbols of this header are the library's only exported symbols. */
 #if defined(__GNUC__)
@@ -70,10 +71,13 @@ BEAM_API const char *beam_status_str(int status);
  * Returns BEAM_ERR_INVALID_ARG for n < 1 or NULL outputs. */
 BEAM_API int beam_residual_scales(int32_t n, float *alpha, float *s);
 
-/* Fault word of the current device.  The persistent boundary kernels (the many-row plain and MoE
- * boundaries) wait on their own bulk copies with a time limit (2 s); a kernel that gives up
- * drains its copies, sets bit 0 (1 = copy wait timed out) and returns without writing valid
- * rows.  Never set in normal operation.
+/* Fault word of the current device.  The persistent boundary kernels (the many-row plain, MoE
+ * and all-reduce boundaries) wait on their own bulk copies with a time limit (2 s).  A CTA whose
+ * wait runs out stops issuing copies, writes nothing from then on (rows it had finished before
+ * keep their new h', y and rstd; the rest keep their previous contents -- an in-place h stays the
+ * old residual stream there), waits (bounded) for its copies still in flight, and sets bit 0
+ * (1 = copy wait timed out).  The call itself has already returned BEAM_OK by then: this word is
+ * the only signal.  Never set in normal operation.
  * Synchronous (a device-to-host copy on the legacy default stream); `clear` != 0 resets the word.
  * No counterpart on the pages: a diagnostic of this library. */
 BEAM_API int beam_device_faults(uint32_t *flags, int clear);
@@ -84,6 +88,19 @@ BEAM_API int beam_device_faults(uint32_t *flags, int clear);
  * persistent kernel whose copies stalled would; nothing is left in flight.  Asynchronous on `stream`;
  * read the result with beam_device_faults().  BEAM_ERR_INVALID_ARG for a limit out of range. */
 BEAM_API int beam_selftest_copy_timeout(int64_t limit_ns, cudaStream_t stream);
+
+/* Diagnostic: runs a persistent boundary kernel -- kind 0: the plain boundary's prefetch kernel;
+ * kind 1: the MoE ring with 8 slots -- with its bulk copies withheld (its barriers are armed, no
+ * copy is issued), so that its waits run out after limit_ns nanoseconds (1 us .. 2 s) exactly as
+ * they would if the copies stalled.  The kernel must then write nothing to h_out, y_out
+ * [T, H] and rstd_out [T, 2] (nullable), and set bit 0 of the device fault word.  The norm
+ * weights w_post, w_pre [H] are read; no other input is.  T in [1, 2^20], H a multiple of 8 in
+ * [8, 8192].  Asynchronous on `stream`.  No counterpart on the pages: a diagnostic of the
+ * persistent kernels' time limit. */
+BEAM_API int beam_selftest_persistent_timeout(int32_t kind, void *h_out, void *y_out,
+                                              float *rstd_out, const void *w_post,
+                                              const void *w_pre, int64_t T, int32_t H,
+                                              int64_t limit_ns, cudaStream_t stream);
 
 /* Host-only helper: the residual operand b = bf16(x / s), s = fp32(sqrt(n)), returned as FP32
  * values, for `count` BF16 values x given as FP32 (low 16 bits zero) in host memory, exactly as
@@ -170,6 +187,31 @@ BEAM_API int beam_moe_combine_boundary_fwd(void *h_out, void *y_out, const void 
                                   float routed_scaling, const void *w_post, const void *w_pre,
                                   int64_t T, int32_t H, int32_t K, int32_t n, float eps,
                                   float *rstd_out, cudaStream_t stream);
+
+/* Tensor-parallel all-reduce of the sublayer output fused ahead of the boundary chain.
+ *
+ * [vLLM] "Agentengetriebene Optimierung", change 3 (both TP all-reduces of every layer run
+ * inside the norm kernel); [SGL] kernel-fusion paragraph (the all-reduce, the output norm, the
+ * scaled residual add and the next layer's input norm fused in one kernel).
+ *
+ * Under tensor parallelism over P ranks each rank holds a partial sublayer output x_p.  Per
+ * token and element, in rank order (FP32 adds, starting from rank 0's value, one rounding):
+ *   x_j = bf16( (((x_{0,j} + x_{1,j}) + x_{2,j}) + ...) + x_{P-1,j} )
+ * then exactly the beam_boundary_fwd chain on x.  With P = 1 the call is beam_boundary_fwd on
+ * x_parts[0].  Every rank that runs it on the same partials gets bit-identical h' and y.
+ *
+ *   x_parts  host array of P device pointers, each a [T, H] bf16 partial (16-byte aligned,
+ *            rows contiguous); the same buffer may appear more than once
+ *   P        in [1, 16]
+ *   other arguments as beam_boundary_fwd.  h_out may be the same buffer as h_in, and y_out may be
+ *   the same buffer as one of the partials; no other overlap.
+ * This call reads the P partials from this GPU's memory.  Gathering the other ranks' partials
+ * (peer copies, or peer-mapped buffers passed here directly) is the caller's. */
+BEAM_API int beam_allreduce_boundary_fwd(void *h_out, void *y_out, const void *h_in,
+                                         const void *const *x_parts, int32_t P,
+                                         const void *w_post, const void *w_pre, int64_t T,
+                                         int32_t H, int32_t n, float eps, float *rstd_out,
+                                         cudaStream_t stream);
 
 /* Per-head Q/K RMSNorm fused with rotary embedding (sliding-window layers), in place.
  *

@@ -21,8 +21,8 @@ from . import _build
 __all__ = ["BeamError", "build", "lib", "beam_abi_version", "beam_status_str",
            "beam_residual_scales", "beam_rope_cos_sin", "beam_residual_operand",
            "beam_exact_square_sum", "beam_routing_sigmoid", "beam_device_faults",
-           "beam_selftest_copy_timeout",
-           "beam_boundary_fwd", "beam_moe_combine_boundary_fwd",
+           "beam_selftest_copy_timeout", "beam_selftest_persistent_timeout",
+           "beam_boundary_fwd", "beam_moe_combine_boundary_fwd", "beam_allreduce_boundary_fwd",
            "beam_qk_norm_rope_fwd", "beam_qk_norm_ssmax_fwd", "beam_qk_norm_rope_kv_fwd",
            "beam_qk_norm_ssmax_kv_fwd", "beam_grouped_topk_fwd", "beam_attn_gate_fwd",
            "HEAD_DIM"]
@@ -65,6 +65,10 @@ def lib() -> ctypes.CDLL:
             so.beam_routing_sigmoid.argtypes = [vp, vp, i64]
             so.beam_device_faults.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
             so.beam_selftest_copy_timeout.argtypes = [i64, vp]
+            so.beam_selftest_persistent_timeout.argtypes = [i32, vp, vp, vp, vp, vp, i64, i32, i64,
+                                                            vp]
+            so.beam_allreduce_boundary_fwd.argtypes = [vp, vp, vp, ctypes.POINTER(vp), i32, vp, vp,
+                                                       i64, i32, i32, f32, vp, vp]
             so.beam_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i32, f32, vp, vp]
             so.beam_moe_combine_boundary_fwd.argtypes = [vp, vp, vp, vp, vp, f32, vp, vp, i64,
                                                          i32, i32, i32, f32, vp, vp]
@@ -83,6 +87,7 @@ def lib() -> ctypes.CDLL:
             for fn in ("beam_abi_version", "beam_residual_scales", "beam_rope_cos_sin",
                        "beam_residual_operand", "beam_exact_square_sum", "beam_routing_sigmoid",
                        "beam_device_faults", "beam_selftest_copy_timeout",
+                       "beam_selftest_persistent_timeout", "beam_allreduce_boundary_fwd",
                        "beam_boundary_fwd",
                        "beam_moe_combine_boundary_fwd", "beam_qk_norm_rope_fwd",
                        "beam_qk_norm_ssmax_fwd", "beam_qk_norm_rope_kv_fwd",
@@ -174,6 +179,25 @@ def beam_selftest_copy_timeout(limit_ns: int = 20_000_000, stream=None) -> None:
     _call("beam_selftest_copy_timeout", limit_ns, _stream(stream))
 
 
+def beam_selftest_persistent_timeout(kind: int, h_out, y_out, w_post, w_pre,
+                                     limit_ns: int = 20_000_000, rstd_out=None,
+                                     stream=None) -> None:
+    """Diagnostic: run a persistent boundary kernel (kind 0: the plain boundary's prefetch kernel;
+    1: the MoE ring) with its bulk copies withheld; its waits run out after limit_ns, it writes
+    nothing to h_out / y_out [T, H] bf16 or rstd_out [T, 2] fp32 and sets bit 0 of the device
+    fault word."""
+    for t, nm in ((h_out, "h_out"), (y_out, "y_out"), (w_post, "w_post"), (w_pre, "w_pre")):
+        _bf16(t, nm)
+    T, H = h_out.shape
+    if y_out.shape != (T, H) or w_post.shape != (H,) or w_pre.shape != (H,):
+        raise ValueError("beam_selftest_persistent_timeout: shape mismatch")
+    if rstd_out is not None:
+        _f32(rstd_out, "rstd_out")
+    with torch.cuda.device(h_out.device):
+        _call("beam_selftest_persistent_timeout", kind, _ptr(h_out), _ptr(y_out), _ptr(rstd_out),
+              _ptr(w_post), _ptr(w_pre), T, H, limit_ns, _stream(stream))
+
+
 def beam_routing_sigmoid(z):
     """Host helper: the FP32 sigmoid the routing kernel ranks experts by (float32 in and out)."""
     import numpy as np
@@ -249,6 +273,34 @@ def beam_moe_combine_boundary_fwd(h_out, y_out, h_in, expert_out, topk_w, w_post
         _call("beam_moe_combine_boundary_fwd", _ptr(h_out), _ptr(y_out), _ptr(h_in),
               _ptr(expert_out), _ptr(topk_w), routed_scaling, _ptr(w_post), _ptr(w_pre), T, H,
               K, n, eps, _ptr(rstd_out), _stream(stream))
+
+
+def beam_allreduce_boundary_fwd(h_out, y_out, h_in, x_parts, w_post, w_pre, n: int,
+                                eps: float = 1e-6, rstd_out=None, stream=None) -> None:
+    """x_parts: a sequence of P [T, H] bf16 tensors (rank p's partial sublayer output), or one
+    [P, T, H] tensor; the rest as beam_boundary_fwd.  The partials are summed in rank order in
+    FP32 and rounded once to BF16 ahead of the boundary chain."""
+    parts = list(x_parts.unbind(0)) if isinstance(x_parts, torch.Tensor) else list(x_parts)
+    for t, nm in ((h_out, "h_out"), (y_out, "y_out"), (h_in, "h_in"), (w_post, "w_post"),
+                  (w_pre, "w_pre")):
+        _bf16(t, nm)
+    T, H = h_in.shape
+    for i, t in enumerate(parts):
+        _bf16(t, f"x_parts[{i}]")
+        if t.shape != (T, H):
+            raise ValueError("beam_allreduce_boundary_fwd: every partial must be [T, H]")
+    if h_out.shape != (T, H) or y_out.shape != (T, H) or w_post.shape != (H,) or \
+            w_pre.shape != (H,):
+        raise ValueError("beam_allreduce_boundary_fwd: shape mismatch")
+    if rstd_out is not None:
+        _f32(rstd_out, "rstd_out")
+        if rstd_out.shape != (T, 2):
+            raise ValueError("rstd_out must be [T, 2]")
+    arr = (ctypes.c_void_p * max(1, len(parts)))(*[t.data_ptr() for t in parts])
+    with torch.cuda.device(h_in.device):
+        _call("beam_allreduce_boundary_fwd", _ptr(h_out), _ptr(y_out), _ptr(h_in), arr,
+              len(parts), _ptr(w_post), _ptr(w_pre), T, H, n, eps, _ptr(rstd_out),
+              _stream(stream))
 
 
 def _heads(t, name):

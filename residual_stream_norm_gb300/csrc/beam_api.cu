@@ -1,8 +1,10 @@
 // beam_api.cu -- C ABI of libbeam_boundary.so: argument checks, host-side coefficients, launch.
 //
 // Every check runs before any CUDA call, so a rejected call launches nothing, touches no output
-// and needs no GPU.  The library holds no state besides a small per-thread cache of RoPE
-// frequency tables; it never allocates device memory and never synchronises.
+// and needs no GPU.  The library holds no state besides small caches (per thread: the RoPE
+// frequency table and the residual rule of the last call; per device: the SM count and the
+// persistent kernels' launch shapes).  It never allocates device memory, and no call
+// synchronises except the beam_device_faults diagnostic.
 
 #include <cmath>
 #include <cstdint>
@@ -14,6 +16,7 @@
 #include "beam_exp.cuh"
 #include "beam_f32x2.cuh"
 #include "beam_sincos.cuh"
+#include "beam_tma.cuh"
 
 namespace {
 
@@ -29,6 +32,14 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? BEAM_OK : BEAM
 int check_hidden(int32_t H) { return (H < 8 || H > kMaxHidden || H % 8 != 0) ? BEAM_ERR_INVALID_ARG : BEAM_OK; }
 
 bool bad_eps(float eps) { return !(eps >= 0.0f) || !std::isfinite(eps); }
+
+// Arguments of a boundary launch with the persistent kernels' usual copy-wait limit.
+beam::BoundaryArgs boundary_args()
+{
+    beam::BoundaryArgs a{};
+    a.wait_ns = beam::kWaitLimitNs;
+    return a;
+}
 
 // fp32(theta^(-2i/128)) for i < 64, formed in double.  Cached per thread for the last theta.
 const float *rope_inv_freq(float theta)
@@ -252,7 +263,7 @@ int beam_boundary_fwd(void *h_out, void *y_out, const void *h_in, const void *x_
     if (!aligned(h_out, 16) || !aligned(y_out, 16) || !aligned(h_in, 16) || !aligned(x_in, 16) ||
         !aligned(w_post, 16) || !aligned(w_pre, 16) || (rstd_out && !aligned(rstd_out, 8)))
         return BEAM_ERR_MISALIGNED;
-    beam::BoundaryArgs a{};
+    beam::BoundaryArgs a = boundary_args();
     a.h_out = h_out;
     a.y_out = y_out;
     a.h_in = h_in;
@@ -286,7 +297,7 @@ int beam_moe_combine_boundary_fwd(void *h_out, void *y_out, const void *h_in,
         !aligned(expert_out, 16) || !aligned(topk_w, 4) || !aligned(w_post, 16) ||
         !aligned(w_pre, 16) || (rstd_out && !aligned(rstd_out, 8)))
         return BEAM_ERR_MISALIGNED;
-    beam::BoundaryArgs a{};
+    beam::BoundaryArgs a = boundary_args();
     a.h_out = h_out;
     a.y_out = y_out;
     a.h_in = h_in;
@@ -303,6 +314,74 @@ int beam_moe_combine_boundary_fwd(void *h_out, void *y_out, const void *h_in,
     beam_residual_scales(n, &a.alpha, &a.s);
     set_residual_rule(a);
     return cuda_status(beam::launch_moe_boundary(a, stream));
+}
+
+int beam_allreduce_boundary_fwd(void *h_out, void *y_out, const void *h_in,
+                                const void *const *x_parts, int32_t P, const void *w_post,
+                                const void *w_pre, int64_t T, int32_t H, int32_t n, float eps,
+                                float *rstd_out, cudaStream_t stream)
+{
+    if (T < 0 || n < 1 || P < 1 || P > beam::kMaxParts || bad_eps(eps) ||
+        check_hidden(H) != BEAM_OK)
+        return BEAM_ERR_INVALID_ARG;
+    if (T == 0)
+        return BEAM_OK;
+    if (!h_out || !y_out || !h_in || !x_parts || !w_post || !w_pre)
+        return BEAM_ERR_INVALID_ARG;
+    for (int32_t p = 0; p < P; ++p)
+        if (!x_parts[p])
+            return BEAM_ERR_INVALID_ARG;
+    if (!aligned(h_out, 16) || !aligned(y_out, 16) || !aligned(h_in, 16) ||
+        !aligned(w_post, 16) || !aligned(w_pre, 16) || (rstd_out && !aligned(rstd_out, 8)))
+        return BEAM_ERR_MISALIGNED;
+    for (int32_t p = 0; p < P; ++p)
+        if (!aligned(x_parts[p], 16))
+            return BEAM_ERR_MISALIGNED;
+    beam::BoundaryArgs a = boundary_args();
+    a.h_out = h_out;
+    a.y_out = y_out;
+    a.h_in = h_in;
+    for (int32_t p = 0; p < P; ++p)
+        a.parts[p] = x_parts[p];
+    a.P = P;
+    a.w_post = w_post;
+    a.w_pre = w_pre;
+    a.rstd_out = rstd_out;
+    a.T = T;
+    a.H = H;
+    a.eps = eps;
+    beam_residual_scales(n, &a.alpha, &a.s);
+    set_residual_rule(a);
+    return cuda_status(beam::launch_allreduce_boundary(a, stream));
+}
+
+int beam_selftest_persistent_timeout(int32_t kind, void *h_out, void *y_out, float *rstd_out,
+                                     const void *w_post, const void *w_pre, int64_t T, int32_t H,
+                                     int64_t limit_ns, cudaStream_t stream)
+{
+    if ((kind != 0 && kind != 1) || T < 1 || T > (int64_t)1 << 20 || limit_ns < 1000 ||
+        limit_ns > 2000000000 || check_hidden(H) != BEAM_OK || H > 8192)
+        return BEAM_ERR_INVALID_ARG;
+    if (!h_out || !y_out || !w_post || !w_pre)
+        return BEAM_ERR_INVALID_ARG;
+    if (!aligned(h_out, 16) || !aligned(y_out, 16) || !aligned(w_post, 16) ||
+        !aligned(w_pre, 16) || (rstd_out && !aligned(rstd_out, 8)))
+        return BEAM_ERR_MISALIGNED;
+    beam::BoundaryArgs a = boundary_args();
+    a.h_out = h_out;
+    a.y_out = y_out;
+    a.w_post = w_post;
+    a.w_pre = w_pre;
+    a.rstd_out = rstd_out;
+    a.T = T;
+    a.H = H;
+    a.K = kind == 1 ? 8 : 0;
+    a.routed_scaling = 1.0f;
+    a.eps = 1e-6f;
+    a.wait_ns = (unsigned long long)limit_ns;
+    beam_residual_scales(2, &a.alpha, &a.s);
+    set_residual_rule(a);
+    return cuda_status(beam::launch_persistent_starved(a, kind == 1, stream));
 }
 
 int beam_qk_norm_rope_fwd(void *q, void *k, int64_t q_row_stride, int64_t k_row_stride,

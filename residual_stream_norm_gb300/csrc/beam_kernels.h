@@ -25,6 +25,9 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Largest number of tensor-parallel partials the all-reduce boundary takes.
+constexpr int kMaxParts = 16;
+
 struct BoundaryArgs {
     void *h_out;
     void *y_out;
@@ -32,12 +35,14 @@ struct BoundaryArgs {
     const void *x_in;        // boundary: sublayer output [T, H]
     const void *expert_out;  // MoE: [T, K, H] (x_in unused)
     const float *topk_w;     // MoE: [T, K]
+    const void *parts[kMaxParts];  // tensor parallel: P partial sublayer outputs [T, H] each
     const void *w_post;
     const void *w_pre;
     float *rstd_out;         // [T, 2] or nullptr
     int64_t T;
     int32_t H;
     int32_t K;               // 0 for the plain boundary
+    int32_t P;               // tensor-parallel partials (0 unless the all-reduce boundary)
     float routed_scaling;
     float alpha;             // fp32(sqrt((n-1)/n))
     float s;                 // fp32(sqrt(n))
@@ -45,6 +50,7 @@ struct BoundaryArgs {
     bool mul_div;            // residual_mul_exact(s, y): b = bf16(x y) where x is above the floor
     uint32_t floor_bits;     // (f << 7) | (f << 23), f = residual_floor_exp(s)
     float eps;
+    unsigned long long wait_ns;  // limit of a persistent kernel's wait on its own copies
 };
 
 struct QkArgs {
@@ -101,6 +107,11 @@ struct GateArgs {
 
 cudaError_t launch_boundary(const BoundaryArgs &a, cudaStream_t stream);
 cudaError_t launch_moe_boundary(const BoundaryArgs &a, cudaStream_t stream);
+cudaError_t launch_allreduce_boundary(const BoundaryArgs &a, cudaStream_t stream);
+// Runs a persistent boundary kernel (moe: the MoE ring with K slots, else the plain boundary's
+// prefetch kernel) with its bulk copies withheld: its first wait runs out after a.wait_ns, it
+// raises the fault word and writes nothing.  a.K is the MoE slot count; inputs are not read.
+cudaError_t launch_persistent_starved(const BoundaryArgs &a, bool moe, cudaStream_t stream);
 cudaError_t launch_qk_norm_rope(const QkArgs &a, cudaStream_t stream);
 cudaError_t launch_qk_norm_ssmax(const QkArgs &a, cudaStream_t stream);
 cudaError_t launch_attn_gate(const GateArgs &a, cudaStream_t stream);

@@ -103,14 +103,15 @@ __device__ __forceinline__ bool mbar_wait_or_fail(uint64_t *bar, uint32_t parity
     return true;
 }
 
-// Wait for phase `parity` of `bar` to complete; false if it did not within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// Wait for phase `parity` of `bar` to complete; false if it did not within `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs)
+        if (global_ns() - t0 > limit_ns)
             return false;
     }
     return true;

@@ -9,9 +9,12 @@
 // "Agentengetriebene Optimierung" change 1; [vLLM] "MoE und Residual-Stream", bullets
 // "Sandwich-Norm" and "Tiefenskalierte Residuen"; [SGL] "三明治归一化与深度缩放残差").  The MoE
 // variant first forms the top-K weighted expert sum ([vLLM] change 3; [SGL] "稠密层与分组 MoE
-// 路由").  Nothing between the stages goes back to HBM: per row the kernel reads x (or the K
-// expert rows) and h once and writes h' and y once; the norm weights come from L1/L2 (rows
-// kernel) or are parked once per CTA in shared memory (ring kernel).
+// 路由"); the tensor-parallel variant first sums the P ranks' partial sublayer outputs (the TP
+// all-reduce that [vLLM] change 3 runs inside the norm kernel, and the [SGL] kernel-fusion
+// paragraph fuses with the norms and the scaled add).  Nothing between the stages goes back to
+// HBM: per row the kernel reads x (or the K expert rows, or the P partial rows) and h once and
+// writes h' and y once; the norm weights come from L1/L2 (rows kernel) or are parked once per
+// CTA in shared memory (persistent kernels).
 //
 // Three layouts, same arithmetic (boundary_chain):
 //  * rows kernel (few tokens, e.g. batch-1 decode): one CTA per token row; each thread owns VPT
@@ -20,17 +23,22 @@
 //    two row buffers in shared memory that one of its threads refills with bulk TMA copies
 //    (cp.async.bulk, completion on an mbarrier) two rows ahead, right after the first block
 //    reduction of the row that leaves the buffer.
-//  * ring kernel (many tokens, MoE variant): a persistent grid with warp specialisation: one
-//    producer warp issues bulk TMA copies of each row's inputs in chunks of 128 vectors -- the K
-//    expert chunks and the h chunk -- into a ring of shared-memory stages, and four consumer
-//    warps reduce and finish the rows, releasing each stage on an "empty" mbarrier as soon as
-//    they have read it.
+//  * ring kernel (many tokens, MoE and tensor-parallel variants): a persistent grid with warp
+//    specialisation: one producer warp issues bulk TMA copies of each row's inputs in chunks of
+//    128 vectors -- the K expert (or P partial) chunks and the h chunk -- into a ring of
+//    shared-memory stages, and four consumer warps reduce and finish the rows, releasing each
+//    stage on an "empty" mbarrier as soon as they have read it.
+// A persistent kernel whose wait on its own copies runs out of time (kernel argument wait_ns)
+// raises the device fault word and from then on writes nothing: no row computed from a buffer
+// that may not have filled reaches h', y or rstd.
 // Only 4 warps share a row, so the two block reductions per row stay cheap, and several CTAs fit
 // on an SM.
 // The row stays in registers as packed BF16 between the two block reductions; element math runs
 // on packed FP32 pairs (beam_f32x2.cuh) with the same IEEE roundings as the scalar definition.
 
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "beam_device.cuh"
 #include "beam_exact.cuh"
@@ -46,7 +54,7 @@ __device__ unsigned int g_fault_word = 0u;
 namespace {
 
 constexpr int kMaxK = 16;
-constexpr int kRingMaxK = 8;  // the MoE ring holds K <= 8 routing coefficients in registers
+constexpr int kRingMaxK = 8;  // the ring takes at most 8 source slots (MoE coefficients in registers)
 
 // Shared-memory slot of one warp in the rare exact path (beam_exact.cuh).
 struct ExactSlot {
@@ -243,14 +251,24 @@ __device__ __forceinline__ uint4 residual_operand_ieee(uint4 xh, float s)
     return b;
 }
 
+// Where a row's sublayer output comes from.
+constexpr int kSrcPlain = 0;  // x_in [T, H]
+constexpr int kSrcMoe = 1;    // the top-K combine of expert_out [T, K, H]
+constexpr int kSrcTp = 2;     // the rank-order sum of the P partials parts[p] [T, H]
+
 // The boundary chain for one row whose inputs sit in registers: xv (x) and hv (h) hold this
 // thread's vectors tid + i * nt.  wpo(i) / wpr(i) give the matching weight vectors.
-// `after_first_sum` runs right after the first block reduction.
+// `after_first_sum` runs right after the first block reduction.  `fail` (persistent kernels;
+// null otherwise) is the CTA's flag that a wait on its own copies ran out.  It is read after the
+// second block reduction, whose barrier follows every thread's waits for this row, and then
+// withholds this row's stores and those of every later row: no output is computed from a buffer
+// that may not have filled.
 template <int VPT, typename WPost, typename WPre, typename AfterFirstSum>
 __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t row,
                                                const uint4 (&xv)[VPT], const uint4 (&hv)[VPT],
                                                WPost wpo, WPre wpr, Sum2 *red,
                                                ExactSlot *xred, float *pred, int nt, bool named,
+                                               const volatile int *fail,
                                                AfterFirstSum after_first_sum)
 {
     const int nvec = a.H >> 3;
@@ -295,6 +313,8 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
         }
     }
     const f2 rr2 = splat(rms_inv(block_sum_sq_plain(hp, pred, nt, named), (float)a.H, a.eps));
+    if (fail != nullptr && *fail != 0)
+        return;  // a wait on this CTA's copies gave up: write nothing
 
     // ---- a3: y = bf16((h' r') w_pre); store h' and y -----------------------------------------
     char *h_out = (char *)a.h_out + 2 * row_off;
@@ -316,12 +336,18 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
         reinterpret_cast<float2 *>(a.rstd_out)[row] = make_float2(r, lo_of(rr2));
 }
 
+template <bool SMEM>
+__device__ __forceinline__ uint4 load_vec(const unsigned char *p)
+{
+    return SMEM ? *reinterpret_cast<const uint4 *>(p) : ld_stream(p);
+}
+
 // x = bf16(sum_k c_k e_k) for one 16-byte vector: one FMA per slot in slot order from +0.
 // `e0` points at slot 0 of this vector; slots are `slot_bytes` apart.
 template <bool SMEM>
 __device__ __forceinline__ void combine_slot(f2 (&acc)[4], float ck, const unsigned char *p)
 {
-    const uint4 ev = SMEM ? *reinterpret_cast<const uint4 *>(p) : ld_stream(p);
+    const uint4 ev = load_vec<SMEM>(p);
     const f2 c2 = splat(ck);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -355,6 +381,40 @@ __device__ __forceinline__ uint4 combine_vec(const float (&c)[KC], int K,
     return x;
 }
 
+// x = bf16(((x_0 + x_1) + x_2) + ... + x_{P-1}) for one 16-byte vector: FP32 adds in rank order
+// starting from rank 0's value, one BF16 rounding.  src(p) points at rank p's vector.
+template <bool SMEM, typename Src>
+__device__ __forceinline__ uint4 reduce_vec(int P, Src src)
+{
+    const uint4 v0 = load_vec<SMEM>(src(0));
+    f2 acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        acc[j] = widen(word(v0, j));
+    if (P == 8) {  // TP8: fully unrolled, every load issued before the adds need it
+#pragma unroll
+        for (int p = 1; p < 8; ++p) {
+            const uint4 v = load_vec<SMEM>(src(p));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                acc[j] = add2(acc[j], widen(word(v, j)));
+        }
+    } else {
+#pragma unroll 1
+        for (int p = 1; p < P; ++p) {
+            const uint4 v = load_vec<SMEM>(src(p));
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                acc[j] = add2(acc[j], widen(word(v, j)));
+        }
+    }
+    uint4 x;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        word(x, j) = narrow(acc[j]);
+    return x;
+}
+
 __device__ __forceinline__ uint4 weight_vec(const void *w, int v, int nvec)
 {
     return v < nvec ? ld_cached((const char *)w + 16 * (int64_t)v) : make_uint4(0u, 0u, 0u, 0u);
@@ -371,7 +431,7 @@ __device__ __forceinline__ void routing_coeffs(const BoundaryArgs &a, int64_t ro
 
 // ---- rows kernel: one CTA per row, inputs straight from memory ------------------------------
 
-template <int VPT, bool MOE>
+template <int VPT, int SRC>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
     boundary_rows_kernel(const BoundaryArgs a)
 {
@@ -395,17 +455,21 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
         const char *h_in = (const char *)a.h_in + 2 * row_off;
         uint4 xv[VPT], hv[VPT];
         float c[kMaxK];
-        if constexpr (MOE)
+        if constexpr (SRC == kSrcMoe)
             routing_coeffs(a, row, c);
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
             const int v = tid + i * nt;
             if (v < nvec) {
                 hv[i] = ld_stream(h_in + 16 * (int64_t)v);
-                if constexpr (MOE)
+                if constexpr (SRC == kSrcMoe)
                     xv[i] = combine_vec<false>(c, a.K, (const unsigned char *)a.expert_out +
                                                            2 * row_off * a.K + 16 * (int64_t)v,
                                                2 * (size_t)a.H);
+                else if constexpr (SRC == kSrcTp)
+                    xv[i] = reduce_vec<false>(a.P, [&](int p) {
+                        return (const unsigned char *)a.parts[p] + 2 * row_off + 16 * (int64_t)v;
+                    });
                 else
                     xv[i] = ld_stream((const char *)a.x_in + 2 * row_off + 16 * (int64_t)v);
             } else {
@@ -415,7 +479,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
         }
         boundary_chain<VPT>(
             a, row, xv, hv, [&](int i) { return wpo[i]; }, [&](int i) { return wpr[i]; }, red,
-            xred, pred, nt, false, [] {});
+            xred, pred, nt, false, nullptr, [] {});
     }
 }
 
@@ -424,21 +488,26 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
 // A CTA has NC consumer threads (a multiple of 32) and one producer warp.  Its rows are
 // blockIdx.x, blockIdx.x + gridDim.x, ...; each row is cut into VPT chunks of NC 16-byte
 // vectors, and consumer thread t owns vector c * NC + t of chunk c.  A unit of work is one chunk
-// of one row; its stage holds the K expert chunks and the h chunk, each NC * 16 bytes.  Per stage two mbarriers: `full` completes when the producer's
+// of one row; its stage holds the row's KIN source chunks (K expert slots, or P partials) and its
+// h chunk, each NC * 16 bytes.  Per stage two mbarriers: `full` completes when the producer's
 // bulk copies have landed (transaction bytes), `empty` when all consumer warps have read the
 // stage (one arrive per warp).  The producer keeps `stages` units in flight.
+//
+// a.starve (the diagnostic beam_selftest_persistent_timeout) arms the `full` barriers without
+// issuing the copies and reads no routing weights: the consumers' first wait runs out after
+// a.wait_ns, and the kernel writes nothing.
 
 constexpr int kRingMaxStages = 4;
 constexpr int kRingHeader = 2 * kRingMaxStages * 8;  // the full and empty mbarriers
 
-// Ring shape of the MoE variant: its stages hold K + 1 slices, so it keeps slices small (4
-// consumer warps) at 3 CTAs per SM.
-constexpr int kMoeConsumers = 128;
-constexpr int kMoeCtasPerSm = 3;
+// Ring shape of the MoE and tensor-parallel variants: their stages hold K + 1 (P + 1) slices,
+// so they keep slices small (4 consumer warps) at 3 CTAs per SM.
+constexpr int kRingConsumers = 128;
+constexpr int kRingCtasPerSm = 3;
 
-template <int NC, int VPT, int MINB>
+template <int NC, int VPT, int MINB, int SRC>
 __global__ void __launch_bounds__(NC + 32, MINB)
-    moe_ring_kernel(const BoundaryArgs a, int stages)
+    ring_kernel(const BoundaryArgs a, int stages, bool starve)
 {
     extern __shared__ __align__(128) unsigned char dyn[];
     uint64_t *full = reinterpret_cast<uint64_t *>(dyn);
@@ -448,11 +517,12 @@ __global__ void __launch_bounds__(NC + 32, MINB)
     __shared__ ExactSlot xred[NC / 32];
     __shared__ float pred[NC / 32];
     __shared__ int fail;
+    volatile int *vfail = &fail;  // written by any thread whose wait runs out
 
     constexpr uint32_t kSlice = NC * 16;
     const int nvec = a.H >> 3;
     const int tid = threadIdx.x;
-    const int KIN = a.K;
+    const int KIN = SRC == kSrcTp ? a.P : a.K;
     const uint32_t stage_bytes = (uint32_t)(KIN + 1) * kSlice;
     // the consumer threads park their slices of w_post and w_pre here ([2][VPT][NC] vectors):
     // read from shared memory inside the chain, they cost no long-latency loads
@@ -484,22 +554,27 @@ __global__ void __launch_bounds__(NC + 32, MINB)
         int st = 0, c = 0;
         uint32_t pass = 0;
         for (int64_t u = 0; u < my_units; ++u) {
+            if (*vfail)
+                break;  // a consumer gave up waiting: issue nothing more
             // the stage's previous use (pass - 1) must have been released by the consumers
-            if (pass > 0 && !mbar_wait_or_fail(&empty[st], (pass - 1) & 1u, &fail))
+            if (pass > 0 && !mbar_wait_or_fail(&empty[st], (pass - 1) & 1u, &fail, a.wait_ns))
                 break;
             const int nv = nvec - c * NC < NC ? nvec - c * NC : NC;
             const uint32_t bytes = (uint32_t)nv * 16u;
             unsigned char *dst = ring + (size_t)st * stage_bytes;
             const size_t col = (size_t)c * kSlice;
             mbar_arrive_expect_tx(&full[st], (uint32_t)(KIN + 1) * bytes);
-            for (int k = 0; k < KIN; ++k) {
-                const char *src =
-                    (const char *)a.expert_out + ((size_t)row * KIN + k) * 2 * a.H;
-                bulk_g2s(dst + (size_t)k * kSlice, src + col, bytes, &full[st]);
+            if (!starve) {
+                for (int k = 0; k < KIN; ++k) {
+                    const char *src =
+                        SRC == kSrcTp ? (const char *)a.parts[k] + (size_t)row * 2 * a.H
+                                      : (const char *)a.expert_out + ((size_t)row * KIN + k) * 2 * a.H;
+                    bulk_g2s(dst + (size_t)k * kSlice, src + col, bytes, &full[st]);
+                }
+                bulk_g2s(dst + (size_t)KIN * kSlice,
+                         (const char *)a.h_in + (size_t)row * 2 * a.H + col, bytes, &full[st]);
+                issued = u + 1;
             }
-            bulk_g2s(dst + (size_t)KIN * kSlice, (const char *)a.h_in + (size_t)row * 2 * a.H + col,
-                     bytes, &full[st]);
-            issued = u + 1;
             if (++c == VPT) {
                 c = 0;
                 row += stride;
@@ -509,10 +584,11 @@ __global__ void __launch_bounds__(NC + 32, MINB)
                 ++pass;
             }
         }
-        // Before leaving, make sure none of this CTA's copies is still landing (bounded).
+        // Before leaving, make sure none of this CTA's copies is still landing (bounded): the
+        // last `stages` units issued, one per stage.
         for (int64_t u = issued - stages > 0 ? issued - stages : 0; u < issued; ++u)
-            (void)mbar_wait(&full[u % stages], (uint32_t)((u / stages) & 1));
-        if (fail)
+            (void)mbar_wait(&full[u % stages], (uint32_t)((u / stages) & 1), a.wait_ns);
+        if (*vfail)
             atomicOr(&g_fault_word, kFaultCopyTimeout);
         return;
     }
@@ -525,27 +601,37 @@ __global__ void __launch_bounds__(NC + 32, MINB)
     }
     pdl_wait();
     const int lane = tid & 31;
-    float c[kRingMaxK], c_next[kRingMaxK];  // this row's and the next row's coefficients
-    if (my_rows > 0)
+    // MoE: this row's and the next row's coefficients
+    float c[kRingMaxK], c_next[kRingMaxK];
+#pragma unroll
+    for (int k = 0; k < kRingMaxK; ++k)
+        c_next[k] = 0.0f;
+    if (SRC == kSrcMoe && my_rows > 0 && !starve)
         routing_coeffs(a, first, c_next);
     int st = 0;          // stage of the next unit
     uint32_t parity = 0;  // phase parity of that stage's `full` barrier for this pass
     for (int64_t i = 0; i < my_rows; ++i) {
         const int64_t row = first + i * stride;
-        // this row's coefficients were fetched during the previous row; fetch the next's
+        if constexpr (SRC == kSrcMoe) {
+            // this row's coefficients were fetched during the previous row; fetch the next's
 #pragma unroll
-        for (int k = 0; k < kRingMaxK; ++k)
-            c[k] = c_next[k];
-        if (i + 1 < my_rows)
-            routing_coeffs(a, row + stride, c_next);
+            for (int k = 0; k < kRingMaxK; ++k)
+                c[k] = c_next[k];
+            if (i + 1 < my_rows && !starve)
+                routing_coeffs(a, row + stride, c_next);
+        }
         uint4 xv[VPT], hv[VPT];
 #pragma unroll
         for (int ch = 0; ch < VPT; ++ch) {
-            (void)mbar_wait_or_fail(&full[st], parity, &fail);
+            (void)mbar_wait_or_fail(&full[st], parity, &fail, a.wait_ns);
             const unsigned char *stage = ring + (size_t)st * stage_bytes;
             if (ch * NC + tid < nvec) {
                 hv[ch] = *reinterpret_cast<const uint4 *>(stage + (size_t)KIN * kSlice + 16 * tid);
-                xv[ch] = combine_vec<true>(c, KIN, stage + 16 * tid, kSlice);
+                if constexpr (SRC == kSrcTp)
+                    xv[ch] = reduce_vec<true>(
+                        KIN, [&](int p) { return stage + (size_t)p * kSlice + 16 * tid; });
+                else
+                    xv[ch] = combine_vec<true>(c, KIN, stage + 16 * tid, kSlice);
             } else {
                 xv[ch] = make_uint4(0u, 0u, 0u, 0u);
                 hv[ch] = xv[ch];
@@ -560,9 +646,10 @@ __global__ void __launch_bounds__(NC + 32, MINB)
         }
         boundary_chain<VPT>(
             a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
-            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, true, [] {});
+            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, true, vfail,
+            [] {});
     }
-    if (tid == 0 && fail)
+    if (tid == 0 && *vfail)
         atomicOr(&g_fault_word, kFaultCopyTimeout);
 }
 
@@ -576,9 +663,14 @@ __global__ void __launch_bounds__(NC + 32, MINB)
 // ahead, so the copies fly during the rest of the row's chain and the next rows'.  With the norm
 // weights parked in shared memory too (WSMEM), a row buffer and the weights take 40 KB for
 // H = 5120, and 4 CTAs of 4 warps fit on an SM at up to 128 registers a thread.
+//
+// Once a wait has run out (the CTA's `fail` flag), thread 0 refills nothing more, so at most one
+// copy per buffer can still be in flight, and the row loop writes nothing.  `starve` (the
+// diagnostic beam_selftest_persistent_timeout) arms the buffers' barriers without issuing the
+// copies.
 
 template <int VPT, int NBUF, bool WSMEM>
-__global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs a)
+__global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs a, bool starve)
 {
     constexpr int NC = 128;
     extern __shared__ __align__(128) unsigned char dyn[];
@@ -587,6 +679,7 @@ __global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs 
     __shared__ ExactSlot xred[32];
     __shared__ float pred[32];
     __shared__ int fail;
+    volatile int *vfail = &fail;  // written by any thread whose wait runs out
     const int nvec = a.H >> 3;
     const int tid = threadIdx.x;
     const uint32_t tbytes = (uint32_t)nvec * 16u;                  // one tensor's row
@@ -599,9 +692,11 @@ __global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs 
     auto issue = [&](int64_t row, int b) {
         unsigned char *dst = dyn + (size_t)b * buf_bytes;
         mbar_arrive_expect_tx(&full[b], 2u * tbytes);
-        bulk_g2s(dst, (const char *)a.x_in + (size_t)row * 2 * a.H, tbytes, &full[b]);
-        bulk_g2s(dst + (size_t)VPT * NC * 16, (const char *)a.h_in + (size_t)row * 2 * a.H,
-                 tbytes, &full[b]);
+        if (!starve) {
+            bulk_g2s(dst, (const char *)a.x_in + (size_t)row * 2 * a.H, tbytes, &full[b]);
+            bulk_g2s(dst + (size_t)VPT * NC * 16, (const char *)a.h_in + (size_t)row * 2 * a.H,
+                     tbytes, &full[b]);
+        }
     };
 
     pdl_launch_dependents();
@@ -624,10 +719,13 @@ __global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs 
         for (int b = 0; b < NBUF && b < my_rows; ++b)
             issue(first + b * stride, b);
 
+    // refills issued by thread 0, one per row from row 0 on (they stop for good once `fail` is
+    // set), so buffer b was filled 1 + |{i < refills : i = b mod NBUF}| times
+    int64_t refills = 0;
     for (int64_t i = 0; i < my_rows; ++i) {
         const int64_t row = first + i * stride;
         const int b = (int)(i % NBUF);
-        (void)mbar_wait_or_fail(&full[b], (uint32_t)((i / NBUF) & 1), &fail);
+        (void)mbar_wait_or_fail(&full[b], (uint32_t)((i / NBUF) & 1), &fail, a.wait_ns);
         const unsigned char *buf = dyn + (size_t)b * buf_bytes;
         uint4 xv[VPT], hv[VPT];
 #pragma unroll
@@ -650,19 +748,22 @@ __global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs 
             [&](int k) {
                 return WSMEM ? wsm[(VPT + k) * NC + tid] : weight_vec(a.w_pre, tid + k * NC, nvec);
             },
-            red, xred, pred, NC, false, [&] {
-                if (tid == 0 && refill)
+            red, xred, pred, NC, false, vfail, [&] {
+                if (tid == 0 && refill && !*vfail) {
                     issue(row + NBUF * stride, b);
+                    ++refills;
+                }
             });
     }
     // Every copy issued was waited for above unless a wait gave up; then make sure none is still
-    // landing before the CTA leaves (bounded), and raise the fault word.
-    if (tid == 0 && fail) {
-        for (int b = 0; b < NBUF; ++b) {
-            const int64_t uses = my_rows > b ? (my_rows - b + NBUF - 1) / NBUF : 0;
-            if (uses > 0)
-                (void)mbar_wait(&full[b], (uint32_t)((uses - 1) & 1));
-        }
+    // landing before the CTA leaves -- the last fill of each buffer (bounded) -- and raise the
+    // fault word.
+    if (tid == 0 && *vfail) {
+        if (!starve)
+            for (int b = 0; b < NBUF && b < my_rows; ++b) {
+                const int64_t fills = 1 + (refills > b ? (refills - b + NBUF - 1) / NBUF : 0);
+                (void)mbar_wait(&full[b], (uint32_t)((fills - 1) & 1), a.wait_ns);
+            }
         atomicOr(&g_fault_word, kFaultCopyTimeout);
     }
 }
@@ -683,25 +784,57 @@ int device_sms()
     return cached_sms;
 }
 
-template <int NC, int VPT, int MINB>
-cudaError_t launch_ring(const BoundaryArgs &a, int stages, size_t smem, int sms,
-                        cudaStream_t stream)
+// Resident blocks per SM of a persistent kernel with `smem` bytes of dynamic shared memory on
+// the current device.  The kernel's dynamic shared-memory limit is raised (never lowered) per
+// (device, kernel), and the occupancy is cached per (device, kernel, smem), so an eager launch
+// pays for neither query after the first.
+cudaError_t persistent_blocks(const void *kern, int threads, size_t smem, int *per_sm)
 {
-    auto kern = moe_ring_kernel<NC, VPT, MINB>;
-    const int threads = NC + 32;
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static std::mutex mu;
+    static std::map<std::pair<int, const void *>, size_t> smem_set;
+    static std::map<std::tuple<int, const void *, size_t>, int> blocks;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto bk = std::make_tuple(dev, kern, smem);
+    const auto it = blocks.find(bk);
+    if (it != blocks.end()) {
+        *per_sm = it->second;
+        return cudaSuccess;
+    }
+    size_t &lim = smem_set[std::make_pair(dev, kern)];
+    if (smem > lim) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        lim = smem;
+    }
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem);
+    if (e != cudaSuccess)
+        return e;
+    blocks[bk] = n;
+    *per_sm = n;
+    return cudaSuccess;
+}
+
+template <int NC, int VPT, int MINB, int SRC>
+cudaError_t launch_ring(const BoundaryArgs &a, int stages, size_t smem, int sms, bool starve,
+                        cudaStream_t stream)
+{
+    auto kern = ring_kernel<NC, VPT, MINB, SRC>;
+    const int threads = NC + 32;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    cudaError_t e = persistent_blocks((const void *)kern, threads, smem, &per_sm);
     if (e != cudaSuccess)
         return e;
     if (per_sm < 1)
         return cudaErrorInvalidConfiguration;
     const int64_t slots = (int64_t)sms * per_sm;
     const unsigned grid = (unsigned)(a.T < slots ? a.T : slots);
-    e = launch_pdl(kern, dim3(grid), dim3(threads), smem, stream, a, stages);
+    e = launch_pdl(kern, dim3(grid), dim3(threads), smem, stream, a, stages, starve);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -721,26 +854,28 @@ int pick_vpt(int nvec, int max_threads)
 
 inline int round_warps(int n) { return (n + 31) / 32 * 32; }
 
-// The MoE ring launch for rows of `chunks` chunks of NC vectors: 3 stages of K + 1 slices beside
-// the parked weights.  For K = 8 and H = 5120 that is 74 KB a CTA, which keeps 3 CTAs on an SM
-// only because the kernel's static arrays are sized for its 4 consumer warps (with a third
-// stage the ring no longer runs dry while the consumers finish a row's chain: 0.93 -> 0.98).
-template <int NC, int MINB>
-cudaError_t launch_ring_chunks(const BoundaryArgs &a, int chunks, int sms, cudaStream_t stream)
+// The ring launch for rows of `chunks` chunks of NC vectors: 3 stages of KIN + 1 slices beside
+// the parked weights.  For 8 slots and H = 5120 that is 74 KB a CTA, which keeps 3 CTAs on an SM
+// only because the kernel's static arrays are sized for its 4 consumer warps (with a third stage
+// the ring no longer runs dry while the consumers finish a row's chain: 0.93 -> 0.98).
+template <int NC, int MINB, int SRC>
+cudaError_t launch_ring_chunks(const BoundaryArgs &a, int chunks, int sms, bool starve,
+                               cudaStream_t stream)
 {
     const int stages = 3;
-    const size_t stage = (size_t)(a.K + 1) * NC * 16;
+    const int kin = SRC == kSrcTp ? a.P : a.K;
+    const size_t stage = (size_t)(kin + 1) * NC * 16;
     const size_t weights = (size_t)2 * chunks * NC * 16;
     const size_t smem = kRingHeader + stages * stage + weights;
     switch (chunks) {
-    case 1: return launch_ring<NC, 1, MINB>(a, stages, smem, sms, stream);
-    case 2: return launch_ring<NC, 2, MINB>(a, stages, smem, sms, stream);
-    case 3: return launch_ring<NC, 3, MINB>(a, stages, smem, sms, stream);
-    case 4: return launch_ring<NC, 4, MINB>(a, stages, smem, sms, stream);
-    case 5: return launch_ring<NC, 5, MINB>(a, stages, smem, sms, stream);
-    case 6: return launch_ring<NC, 6, MINB>(a, stages, smem, sms, stream);
-    case 7: return launch_ring<NC, 7, MINB>(a, stages, smem, sms, stream);
-    default: return launch_ring<NC, 8, MINB>(a, stages, smem, sms, stream);
+    case 1: return launch_ring<NC, 1, MINB, SRC>(a, stages, smem, sms, starve, stream);
+    case 2: return launch_ring<NC, 2, MINB, SRC>(a, stages, smem, sms, starve, stream);
+    case 3: return launch_ring<NC, 3, MINB, SRC>(a, stages, smem, sms, starve, stream);
+    case 4: return launch_ring<NC, 4, MINB, SRC>(a, stages, smem, sms, starve, stream);
+    case 5: return launch_ring<NC, 5, MINB, SRC>(a, stages, smem, sms, starve, stream);
+    case 6: return launch_ring<NC, 6, MINB, SRC>(a, stages, smem, sms, starve, stream);
+    case 7: return launch_ring<NC, 7, MINB, SRC>(a, stages, smem, sms, starve, stream);
+    default: return launch_ring<NC, 8, MINB, SRC>(a, stages, smem, sms, starve, stream);
     }
 }
 
@@ -752,71 +887,70 @@ constexpr int kPfBuffers = 2;
 constexpr bool kPfWeightsInSmem = true;
 
 template <int VPT>
-cudaError_t launch_pf_vpt(const BoundaryArgs &a, int sms, cudaStream_t stream)
+cudaError_t launch_pf_vpt(const BoundaryArgs &a, int sms, bool starve, cudaStream_t stream)
 {
     auto kern = boundary_pf_kernel<VPT, kPfBuffers, kPfWeightsInSmem>;
     const size_t smem = (size_t)kPfBuffers * 2 * VPT * 128 * 16 +
                         (kPfWeightsInSmem ? (size_t)2 * VPT * 128 * 16 : 0);
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
-        return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 128, smem);
+    cudaError_t e = persistent_blocks((const void *)kern, 128, smem, &per_sm);
     if (e != cudaSuccess)
         return e;
     if (per_sm < 1)
         return cudaErrorInvalidConfiguration;
     const int64_t slots = (int64_t)sms * per_sm;
     const unsigned grid = (unsigned)(a.T < slots ? a.T : slots);
-    e = launch_pdl(kern, dim3(grid), dim3(128), smem, stream, a);
+    e = launch_pdl(kern, dim3(grid), dim3(128), smem, stream, a, starve);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_pf(const BoundaryArgs &a, int chunks, int sms, cudaStream_t stream)
+cudaError_t launch_pf(const BoundaryArgs &a, int chunks, int sms, bool starve,
+                      cudaStream_t stream)
 {
     switch (chunks) {
-    case 1: return launch_pf_vpt<1>(a, sms, stream);
-    case 2: return launch_pf_vpt<2>(a, sms, stream);
-    case 3: return launch_pf_vpt<3>(a, sms, stream);
-    case 4: return launch_pf_vpt<4>(a, sms, stream);
-    case 5: return launch_pf_vpt<5>(a, sms, stream);
-    case 6: return launch_pf_vpt<6>(a, sms, stream);
-    case 7: return launch_pf_vpt<7>(a, sms, stream);
-    default: return launch_pf_vpt<8>(a, sms, stream);
+    case 1: return launch_pf_vpt<1>(a, sms, starve, stream);
+    case 2: return launch_pf_vpt<2>(a, sms, starve, stream);
+    case 3: return launch_pf_vpt<3>(a, sms, starve, stream);
+    case 4: return launch_pf_vpt<4>(a, sms, starve, stream);
+    case 5: return launch_pf_vpt<5>(a, sms, starve, stream);
+    case 6: return launch_pf_vpt<6>(a, sms, starve, stream);
+    case 7: return launch_pf_vpt<7>(a, sms, starve, stream);
+    default: return launch_pf_vpt<8>(a, sms, starve, stream);
     }
 }
 
-template <bool MOE>
+template <int SRC>
 cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
 {
     const int nvec = a.H / 8;
     const int sms = device_sms();
     // Many rows (and rows of at most 8 chunks of 128 vectors): the persistent kernels, the
-    // prefetch kernel for the plain boundary and the warp-specialised TMA ring for the MoE
-    // variant.
+    // prefetch kernel for the plain boundary and the warp-specialised TMA ring for the MoE and
+    // tensor-parallel variants (at most 8 source slots a row).
     const int chunks = (nvec + 127) / 128;
-    if (a.T >= 4 * (int64_t)sms && chunks <= 8 && (!MOE || a.K <= kRingMaxK)) {
-        if constexpr (MOE)
-            return launch_ring_chunks<kMoeConsumers, kMoeCtasPerSm>(a, chunks, sms, stream);
+    const int slots = SRC == kSrcMoe ? a.K : (SRC == kSrcTp ? a.P : 0);
+    if (a.T >= 4 * (int64_t)sms && chunks <= 8 && slots <= kRingMaxK) {
+        if constexpr (SRC == kSrcPlain)
+            return launch_pf(a, chunks, sms, false, stream);
         else
-            return launch_pf(a, chunks, sms, stream);
+            return launch_ring_chunks<kRingConsumers, kRingCtasPerSm, SRC>(a, chunks, sms, false,
+                                                                            stream);
     }
-    // Few rows (or very wide rows): one CTA per row straight from memory.
+    // Few rows (or very wide rows, or more than 8 slots): one CTA per row straight from memory.
     // Blocks of at most 512 threads for few rows (320 for H = 5120, two vectors a thread: a
     // decode boundary took 2.74 us in a CUDA graph, against 3.13 us with 640 threads of one
     // vector and 3.22 us with 160 of four), 256 or 320 otherwise.
     const bool small = a.T < 2 * (int64_t)sms;
-    const int max_threads = small ? 512 : (MOE ? 320 : 256);
+    const int max_threads = small ? 512 : (SRC == kSrcPlain ? 256 : 320);
     const int vpt = pick_vpt(nvec, max_threads);
     const int threads = round_warps((nvec + vpt - 1) / vpt);
     const dim3 grid((unsigned)(a.T < (int64_t)(1 << 30) ? a.T : (int64_t)(1 << 30)));
     cudaError_t e;
     switch (vpt) {
-    case 1: e = launch_pdl(boundary_rows_kernel<1, MOE>, grid, dim3(threads), 0, stream, a); break;
-    case 2: e = launch_pdl(boundary_rows_kernel<2, MOE>, grid, dim3(threads), 0, stream, a); break;
-    case 4: e = launch_pdl(boundary_rows_kernel<4, MOE>, grid, dim3(threads), 0, stream, a); break;
-    default: e = launch_pdl(boundary_rows_kernel<8, MOE>, grid, dim3(threads), 0, stream, a); break;
+    case 1: e = launch_pdl(boundary_rows_kernel<1, SRC>, grid, dim3(threads), 0, stream, a); break;
+    case 2: e = launch_pdl(boundary_rows_kernel<2, SRC>, grid, dim3(threads), 0, stream, a); break;
+    case 4: e = launch_pdl(boundary_rows_kernel<4, SRC>, grid, dim3(threads), 0, stream, a); break;
+    default: e = launch_pdl(boundary_rows_kernel<8, SRC>, grid, dim3(threads), 0, stream, a); break;
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -825,12 +959,27 @@ cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
 
 cudaError_t launch_boundary(const BoundaryArgs &a, cudaStream_t stream)
 {
-    return launch<false>(a, stream);
+    return launch<kSrcPlain>(a, stream);
 }
 
 cudaError_t launch_moe_boundary(const BoundaryArgs &a, cudaStream_t stream)
 {
-    return launch<true>(a, stream);
+    return launch<kSrcMoe>(a, stream);
+}
+
+cudaError_t launch_allreduce_boundary(const BoundaryArgs &a, cudaStream_t stream)
+{
+    return launch<kSrcTp>(a, stream);
+}
+
+cudaError_t launch_persistent_starved(const BoundaryArgs &a, bool moe, cudaStream_t stream)
+{
+    const int chunks = (a.H / 8 + 127) / 128;
+    const int sms = device_sms();
+    if (moe)
+        return launch_ring_chunks<kRingConsumers, kRingCtasPerSm, kSrcMoe>(a, chunks, sms, true,
+                                                                            stream);
+    return launch_pf(a, chunks, sms, true, stream);
 }
 
 namespace {

@@ -1,4 +1,4 @@
-"""Helpers for the GPU parity tests: device placement, guard bands, row sampling."""
+"""Helpers for the GPU parity tests: device placement, guard bands, launch-shape row counts."""
 from __future__ import annotations
 
 import numpy as np
@@ -37,11 +37,9 @@ class Guarded:
         assert bool((lo == CANARY).all()) and bool((hi == CANARY).all()), "guard band overwritten"
 
 
-def sample_rows(T: int, count: int, seed: int = 0, must=()) -> np.ndarray:
-    g = np.random.Generator(np.random.PCG64(seed))
-    rows = set(int(r) for r in must if 0 <= r < T) | {0, T - 1}
-    rows |= set(int(r) for r in g.choice(T, size=min(count, T), replace=False))
-    return np.array(sorted(rows), dtype=np.int64)
+def persistent_T() -> int:
+    """A row count just above the switch to the persistent kernels (4 rows per SM)."""
+    return 4 * torch.cuda.get_device_properties(0).multi_processor_count + 5
 
 
 def u16(t):

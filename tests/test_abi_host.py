@@ -37,14 +37,14 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 17, names
+    assert len(names) == 19, names
     raw = ctypes.CDLL(rsn.LIB_PATH)
     for nm in names:
         assert hasattr(raw, nm), f"{nm} declared in the header but not exported"
 
 
 def test_version_and_status_strings(lib):
-    assert rsn.beam_abi_version() == 1
+    assert rsn.beam_abi_version() == 2
     assert rsn.beam_status_str(0) == "BEAM_OK"
     assert rsn.beam_status_str(-2) == "BEAM_ERR_MISALIGNED"
     assert rsn.beam_status_str(42) == "unknown"
@@ -86,6 +86,36 @@ def moe(lib, K=8, topk=A, scale=2.5, T=4, e=B, **kw):
 ])
 def test_moe_argument_checks(lib, kw, want):
     assert moe(lib, **kw) == want
+
+
+def allreduce(lib, parts=(A, B, A, B), P=None, T=4, H=5120, n=5, h_out=A, y_out=B,
+              rstd=None):
+    arr = (ctypes.c_void_p * max(1, len(parts)))(*parts)
+    return lib.beam_allreduce_boundary_fwd(h_out, y_out, A, arr, len(parts) if P is None else P,
+                                           A, B, T, H, n, 1e-6, rstd, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(P=0), INVALID), (dict(P=17), INVALID), (dict(T=-1), INVALID), (dict(n=0), INVALID),
+    (dict(H=12), INVALID), (dict(parts=(A, None, B)), INVALID), (dict(h_out=None), INVALID),
+    (dict(parts=(A, B + 8)), MISALIGNED), (dict(y_out=B + 2), MISALIGNED),
+    (dict(rstd=U + 4), MISALIGNED), (dict(T=0), OK),
+    # 16 partials (the same buffer may repeat) pass the checks; with T = 0 nothing launches
+    (dict(parts=(A,) * 16, T=0), OK),
+])
+def test_allreduce_argument_checks(lib, kw, want):
+    assert allreduce(lib, **kw) == want
+
+
+def test_persistent_timeout_selftest_argument_checks(lib):
+    f = lib.beam_selftest_persistent_timeout
+    assert f(2, A, B, None, A, B, 4, 5120, 10**6, None) == INVALID      # kind
+    assert f(0, A, B, None, A, B, 0, 5120, 10**6, None) == INVALID      # T
+    assert f(0, A, B, None, A, B, 4, 16384, 10**6, None) == INVALID     # H > 8192
+    assert f(1, A, B, None, A, B, 4, 5120, 10, None) == INVALID         # limit
+    assert f(0, None, B, None, A, B, 4, 5120, 10**6, None) == INVALID
+    assert f(0, A + 8, B, None, A, B, 4, 5120, 10**6, None) == MISALIGNED
+    assert f(0, A, B, U + 4, A, B, 4, 5120, 10**6, None) == MISALIGNED
 
 
 def qk(lib, fn="rope", q=A, k=B, qs=48 * 128, ks=8 * 128, pos=U, T=4, nq=48, nk=8, D=128,

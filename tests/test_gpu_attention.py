@@ -301,3 +301,75 @@ def test_dependent_chain_across_kernels():
         assert_bf16_close(u16(ys[p]), oy, what=f"chain y, pass {p}")
     assert_bf16_close(u16(q), oq, what="chain q")
     assert_bf16_close(u16(h), oh, what="chain h")
+
+def _tie_heads(T, nh, seed, nudge_every=2):
+    """Heads [T, nh, 128] whose sum of squares is an FP32 rounding midpoint exactly, or (every
+    `nudge_every`-th head) lies just above one: four large elements +-a, one in each lane's
+    vectors (vectors 0..3 belong to lanes 0..3 of the head's quad), so S0 = 4 a^2; small
+    elements b, spread over all four lanes, adding exactly half an FP32 ulp of S0; and, for the
+    nudged heads, a tiny t with t^2 ~ 2^-60 S0.  A plain or compensated FP32 sum rounds every one
+    of them to S0; the exact sum rounds the nudged ones up.  a varies from head to head, so a sum
+    taken from another quad, or one that misses a lane, moves r by far more than a BF16 ulp."""
+    from fractions import Fraction
+    g = np.random.Generator(np.random.PCG64(seed))
+    x = np.zeros((T, nh, D), np.float32)
+    for t in range(T):
+        for h in range(nh):
+            m, e = (t * 7 + h * 3) % 8, (t + h) % 6 - 3
+            a = np.float32((1 + m / 8) * 2.0 ** e)
+            s0 = Fraction(4) * Fraction(float(a)) ** 2
+            E = int(np.floor(np.log2(float(s0))))
+            if E % 2 == 0:
+                nb, b = 16, np.float32(2.0 ** ((E - 28) // 2))    # 16 b^2 = 2^(E-24)
+            else:
+                nb, b = 8, np.float32(2.0 ** ((E - 27) // 2))     # 8 b^2 = 2^(E-24)
+            off = h % 8
+            sign = lambda: np.float32(1.0 if g.random() < 0.5 else -1.0)  # noqa: E731
+            for v in range(4):
+                x[t, h, 8 * v + off] = sign() * a
+            for i in range(nb):
+                x[t, h, 8 * i + (off + 1) % 8] = sign() * b
+            nudged = (t * nh + h) % nudge_every == 0
+            if nudged:
+                x[t, h, 120 + (off + 2) % 8] = np.float32(2.0 ** (E // 2 - 30))
+            if (t * nh + h) % 13 == 0:
+                # the construction: S = S0 + ulp(S0)/2 (+ t^2), an FP32 midpoint (or just above)
+                ssum = sum(Fraction(float(v)) ** 2 for v in x[t, h])
+                half = Fraction(2) ** (E - 24)
+                assert ssum - s0 == half + (Fraction(float(2.0 ** (E // 2 - 30))) ** 2
+                                            if nudged else 0)
+    return oracle.bf16_rne(x)
+
+
+@pytest.mark.parametrize("T,nq,nk", [(5, 48, 8), (5, 3, 2), (4, 5, 0), (3, 1, 1),
+                                     (4 * 152 + 3, 48, 8), (4 * 152 + 3, 3, 2),
+                                     (4 * 152 + 5, 1, 1)])
+def test_near_tie_heads_in_every_quad_position(T, nq, nk):
+    # RoPE head sums at an FP32 rounding midpoint, in every quad position of every warp, beside
+    # inactive quads (head counts that leave a pass ragged: 3 + 2, 5 + 0, 1 + 1 heads, and a last
+    # tile of 3 or 5 tokens) and, through the KV-cache kernel, beside V quads that take another
+    # path.  Only the exact path rounds the nudged heads right, so the outputs are bit-identical
+    # to the oracle only if that path runs, in every lane configuration, on its own quad's data.
+    c = bi.attn_qk_case(T=T, n_q=nq, n_kv=nk, seed=T + nq + nk)
+    c["q"] = bi.from_u16(_tie_heads(T, nq, seed=1)) if nq else c["q"]
+    c["k"] = bi.from_u16(_tie_heads(T, nk, seed=2)) if nk else c["k"]
+    wq, wk = oracle_qk("rope", c)
+    q = dev(c["q"]) if nq else torch.empty((T, 0, D), dtype=torch.bfloat16, device="cuda")
+    k = dev(c["k"]) if nk else torch.empty((T, 0, D), dtype=torch.bfloat16, device="cuda")
+    qo, ko = run_qk("rope", c, q=q, k=k)
+    assert np.array_equal(u16(qo), wq) and np.array_equal(u16(ko), wk), "rope"
+    if nk == 0:
+        return
+    # the same heads through the KV-cache kernel (V quads interleaved with the norm quads)
+    kv = bi.kv_cache_case(T=T, n_kv=nk, seed=T, pad_frac=0.1, oob_frac=0.05)
+    q2 = dev(c["q"]) if nq else torch.empty((T, 0, D), dtype=torch.bfloat16, device="cuda")
+    k2 = dev(c["k"])
+    kc = torch.zeros((kv["num_slots"], nk, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    rsn.beam_qk_norm_rope_kv_fwd(q2, k2, dev(kv["v"]), dev(c["wq"]), dev(c["wk"]),
+                                 dev(c["pos"]), dev(kv["slot_mapping"]), kc, vc)
+    torch.cuda.synchronize()
+    okc, ovc = oracle.kv_cache_write(np.zeros(kc.shape, np.uint16), np.zeros(vc.shape, np.uint16),
+                                     wk, u16(kv["v"]), kv["slot_mapping"].numpy())
+    assert np.array_equal(u16(q2), wq) and np.array_equal(u16(k2), wk), "rope + kv"
+    assert np.array_equal(u16(kc), okc) and np.array_equal(u16(vc), ovc), "kv cache"

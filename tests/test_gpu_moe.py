@@ -11,7 +11,7 @@ import torch
 import beam_inputs as bi
 import oracle
 import residual_stream_norm_gb300 as rsn
-from tests._gpu import Guarded, dev, lib, sample_rows, u16
+from tests._gpu import Guarded, dev, lib, persistent_T, u16
 from tests._util import assert_bf16_close
 
 pytestmark = pytest.mark.gpu
@@ -85,8 +85,9 @@ def test_scale_and_weight_variants():
     check(run_gpu(c["h"], c["e"], w, c["w_post"], c["w_pre"], 9), oracle_run(c1, n=9), "one-hot")
 
 
-def test_prefill_16384_sampled_rows():
-    # 8 x 2048 prefill MoE variant, full size: e [16384, 8, 5120] (1.34 GB).
+def test_prefill_16384_every_row():
+    # 8 x 2048 prefill MoE variant, full size: e [16384, 8, 5120] (1.34 GB); the oracle recomputes
+    # every row (token slices on the host cores).
     c = bi.moe_case(T=16384, seed=1)
     T = 16384
     h = dev(c["h"])
@@ -97,16 +98,22 @@ def test_prefill_16384_sampled_rows():
     rsn.beam_moe_combine_boundary_fwd(h_out, y, h, e, w, dev(c["w_post"]), dev(c["w_pre"]),
                                       c["n"], bi.EPS, bi.ROUTED_SCALING, rstd)
     torch.cuda.synchronize()
-    rows = sample_rows(T, 40, seed=2)
-    want = oracle.moe_combine_boundary(u16(c["h"][rows]), u16(c["e"][rows]),
-                                       c["topk_w"][rows].numpy(), u16(c["w_post"]),
-                                       u16(c["w_pre"]), c["n"])
-    check((u16(h_out[rows]), u16(y[rows]), rstd[rows].cpu().numpy()), want, "prefill MoE")
+    hu, eu, wn = u16(c["h"]), u16(c["e"]), c["topk_w"].numpy()
+    wpo, wpr = u16(c["w_post"]), u16(c["w_pre"])
+    parts = oracle.run_token_parallel(
+        lambda lo, hi: oracle.moe_combine_boundary(hu[lo:hi], eu[lo:hi], wn[lo:hi], wpo, wpr,
+                                                   c["n"]), T, 16)
+    want = tuple(np.concatenate([p[i] for p in parts]) for i in range(3))
+    check((u16(h_out), u16(y), rstd.cpu().numpy()), want, "prefill MoE")
 
 
-def test_in_place_residual_and_guards():
-    c = bi.moe_case(T=21, seed=6)
-    T, K, H = c["e"].shape
+@pytest.mark.parametrize("which", ["rows", "persistent"])
+def test_in_place_residual_and_guards(which):
+    # h' over h with guard bands; "persistent" takes T = 4 SMs + 5 rows, just enough for the TMA
+    # ring, whose producer copies later rows while the consumers write earlier ones back
+    T = 21 if which == "rows" else persistent_T()
+    c = bi.moe_case(T=T, seed=6)
+    _, K, H = c["e"].shape
     want = oracle_run(c)
     h = Guarded((T, H), fill=dev(c["h"]))
     y = Guarded((T, H))
@@ -115,8 +122,8 @@ def test_in_place_residual_and_guards():
     torch.cuda.synchronize()
     h.check()
     y.check()
-    assert_bf16_close(u16(h.view), want[0], what="in-place h'")
-    assert_bf16_close(u16(y.view), want[1], what="y")
+    assert_bf16_close(u16(h.view), want[0], what=f"in-place h' ({which})")
+    assert_bf16_close(u16(y.view), want[1], what=f"y ({which})")
 
 
 def test_zero_tokens():
