@@ -19,6 +19,7 @@ the units are independent tokens, so N ranks process N batches ("weak" scaling).
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -57,10 +58,27 @@ KERNELS = list(BYTES_PER_TOKEN)
 KV_BYTES_PER_TOKEN = BYTES_PER_TOKEN["qk_norm_rope"] + NKV * D * 2 + 8 + 2 * NKV * D
 # Grouped routing: 256 FP32 logits read, 8 int32 ids and 8 FP32 weights written.
 ROUTE_BYTES_PER_TOKEN = bi.N_EXPERTS * 4 + K * 4 + K * 4
+# The boundary with the tensor-parallel all-reduce fused ahead of it (TP8): the 8 partials and h
+# read, h' and y written.
+TP = bi.TP_RANKS
+ALLREDUCE_BYTES_PER_TOKEN = (TP + 1) * H * 2 + 2 * H * 2
+# Launches per kernel in the isolated timings (independent of --steps).
+ISOLATED_LAUNCHES = 300
 SOURCES = {
     "qk_norm_rope": "attention.cu", "qk_norm_ssmax": "attention.cu", "attn_gate": "attention.cu",
     "boundary": "boundary.cu", "moe_combine_boundary": "boundary.cu",
 }
+
+
+def bench_config(ws: int) -> dict:
+    """The workload description both arms print (identical keys and values)."""
+    return {"workload": "prefill 8x2048 = 16384 tokens at ~100K context: one pass of "
+                        "qk_norm_rope, qk_norm_ssmax, attn_gate, boundary, "
+                        "moe_combine_boundary (hidden 5120, 48/8 heads x 128, top-8)",
+            "tokens_per_step": T_PREFILL, "hidden": H, "top_k": K,
+            "l2": "inputs larger than L2 (every kernel streams >= 168 MB per launch; "
+                  "L2 129 MB); no flush",
+            "parallelism": f"replicas x{ws}"}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -220,13 +238,12 @@ class Step:
         layer = i % 52
         return 2 * layer + 1, 2 * layer + 2
 
-    def launch(self, i: int, events=None) -> int:
-        """Launch the five kernels of step i on the current stream; returns launches."""
-        d, L, st = self.dev, self.lib, torch.cuda.current_stream().cuda_stream
+    def calls(self, i: int, st: int) -> tuple:
+        """(entry point, arguments) of the five kernels of step i on the stream handle st."""
+        d = self.dev
         n_attn, n_ffn = self.n_pair(i)
         wi = (n_attn - 1) % bi.N_BOUNDARIES
-        rec = events.__getitem__ if events is not None else None
-        calls = (
+        return (
             ("beam_qk_norm_rope_fwd", (d["q_r"].data_ptr(), d["k_r"].data_ptr(), NQ * D, NKV * D,
                                         d["wq_r"].data_ptr(), d["wk_r"].data_ptr(),
                                         d["pos_r"].data_ptr(), self.T, NQ, NKV, D, bi.EPS,
@@ -248,6 +265,12 @@ class Step:
                                                 d["w_post_m"].data_ptr(), d["w_pre_m"].data_ptr(),
                                                 self.T, H, K, n_ffn, bi.EPS, None, st)),
         )
+
+    def launch(self, i: int, events=None) -> int:
+        """Launch the five kernels of step i on the current stream; returns launches."""
+        L, st = self.lib, torch.cuda.current_stream().cuda_stream
+        rec = events.__getitem__ if events is not None else None
+        calls = self.calls(i, st)
         for j, (fn, args) in enumerate(calls):
             if rec is not None:
                 rec(j).record()
@@ -257,6 +280,15 @@ class Step:
         if rec is not None:
             rec(len(calls)).record()
         return len(calls)
+
+    def kernel(self, j: int):
+        """A closure that launches kernel j of step 0 alone on the current stream."""
+        def run():
+            fn, args = self.calls(0, torch.cuda.current_stream().cuda_stream)[j]
+            stt = getattr(self.lib, fn)(*args)
+            if stt != 0:
+                raise RuntimeError(f"{fn} returned {stt}")
+        return run
 
     def outputs(self):
         d = self.dev
@@ -290,8 +322,8 @@ def source_hash(name: str) -> str:
 
 
 def profiled_traffic(name: str, T: int):
-    """DRAM bytes per launch from the committed ncu summary, scaled to T tokens; None when the
-    kernel source changed since the counters were taken."""
+    """DRAM bytes (read + write, read, write) per launch from the committed ncu capture, scaled to
+    T tokens; None when the kernel source changed since the counters were taken."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
@@ -300,7 +332,14 @@ def profiled_traffic(name: str, T: int):
         return None
     if rec.get("source_sha") != source_hash(name):
         return None
-    return float(rec["dram_bytes_per_token"]) * T
+    per = T / float(rec["tokens_captured"])
+    rd, wr = rec["dram_read_mb"] * 1e6 * per, rec["dram_write_mb"] * 1e6 * per
+    return {"traffic": round(rd + wr, 1), "traffic_read": round(rd, 1),
+            "traffic_write": round(wr, 1),
+            "traffic_note": (f"ncu dram__bytes_read.sum / dram__bytes_write.sum of one launch at "
+                             f"T={rec['tokens_captured']}, scaled to T={T}; reads match the "
+                             "algorithmic input bytes, writes fall short by what is still dirty "
+                             "in L2 when the kernel ends (not counted by the DRAM counters)")}
 
 
 # ---------------------------------------------------------------------------------------------
@@ -423,7 +462,251 @@ def decode_chain_us(device, replays: int = 200) -> dict:
             "T": 1, "note": "working set fits in L2: time only, no HBM GB/s"}
 
 
-def next_rows(host: dict, device, peak: float, iters: int = 50) -> dict:
+def time_isolated(fn, launches: int, device) -> float:
+    """Mean ms per launch of `fn` over `launches` back-to-back launches on the current stream
+    (after 5 warm-up launches), timed with CUDA events on that stream."""
+    for _ in range(5):
+        fn()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e0.record()
+    for _ in range(launches):
+        fn()
+    e1.record()
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1) / launches
+
+
+def graph_us(seq, replays: int, device) -> float:
+    """Microseconds per replay of one CUDA graph that captures seq(stream_handle), warm; the
+    launches inside are back to back with programmatic dependent launch."""
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        seq(s.cuda_stream)  # warm: first launches set up their kernels outside the capture
+        with torch.cuda.graph(g, stream=s):
+            seq(s.cuda_stream)
+    torch.cuda.synchronize(device)
+    for _ in range(10):
+        g.replay()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(replays):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1) * 1e3 / replays
+
+
+def kernel_row(name: str, ms: float, by_per_token: int, T: int, peak: float) -> dict:
+    by = by_per_token * T
+    gbs = by / (ms * 1e-3) / 1e9
+    return {"us": round(ms * 1e3, 2), "bytes_per_launch": by, "gb_s": round(gbs, 1),
+            "frac_of_peak": round(gbs / peak, 4), "tokens_per_s": round(T / (ms * 1e-3), 1)}
+
+
+def isolated_kernels(step: "Step", device, peak: float) -> dict:
+    """Each kernel of the step timed alone over ISOLATED_LAUNCHES launches of its own at
+    T = 16384 (inputs larger than L2, so no launch finds the previous one's data in L2)."""
+    out = {}
+    for j, name in enumerate(KERNELS):
+        ms = time_isolated(step.kernel(j), ISOLATED_LAUNCHES, device)
+        out[name] = kernel_row(name, ms, BYTES_PER_TOKEN[name], step.T, peak)
+        out[name]["launches"] = ISOLATED_LAUNCHES
+    return out
+
+
+def allreduce_rows(device, peak: float) -> dict:
+    """The boundary with the TP8 all-reduce fused ahead of it: T = 16384 (HBM roofline, the 8
+    partials in this GPU's memory) timed alone, and the decode sizes T = 1 and T = 128 in CUDA
+    graphs of 100 launches (L2-resident: time only)."""
+    import residual_stream_norm_gb300 as rsn
+    L = rsn.lib()
+    out = {}
+    c = bi.allreduce_case(T=T_PREFILL, P=TP, n=31, seed=11)
+    h = c["h"].to(device)
+    parts = c["parts"].to(device)
+    del c
+    y = torch.empty_like(h)
+    ptrs = (ctypes.c_void_p * TP)(*[parts[p].data_ptr() for p in range(TP)])
+    wpo = bi.norm_weight(bi.rng(12), H).to(device)
+    wpr = bi.norm_weight(bi.rng(13), H).to(device)
+
+    def launch(T, hh, yy, pp, st):
+        stt = L.beam_allreduce_boundary_fwd(hh.data_ptr(), yy.data_ptr(), hh.data_ptr(), pp, TP,
+                                            wpo.data_ptr(), wpr.data_ptr(), T, H, 31, bi.EPS,
+                                            None, st)
+        if stt != 0:
+            raise RuntimeError(f"beam_allreduce_boundary_fwd returned {stt}")
+
+    ms = time_isolated(lambda: launch(T_PREFILL, h, y, ptrs,
+                                      torch.cuda.current_stream(device).cuda_stream),
+                       ISOLATED_LAUNCHES, device)
+    out["prefill_T16384_tp8"] = kernel_row("allreduce_boundary", ms, ALLREDUCE_BYTES_PER_TOKEN,
+                                           T_PREFILL, peak)
+    out["prefill_T16384_tp8"].update(launches=ISOLATED_LAUNCHES, partials=TP,
+                                     bytes_per_token=ALLREDUCE_BYTES_PER_TOKEN)
+    for T in (1, 128):
+        hs, ys = h[:T].clone(), y[:T].clone()
+        pt = (ctypes.c_void_p * TP)(*[parts[p, :T].data_ptr() for p in range(TP)])
+        us = graph_us(lambda st: [launch(T, hs, ys, pt, st) for _ in range(100)], 50,
+                      device) / 100
+        out[f"decode_T{T}_tp8"] = {"us": round(us, 3), "tokens_per_s": round(T / (us * 1e-6), 1),
+                                   "note": "CUDA graph of 100 launches; L2-resident: time only"}
+    del parts
+    return out
+
+
+def small_configs(device) -> dict:
+    """The workload's small configurations, each timed as CUDA graphs of back-to-back launches
+    (warm; their working sets fit in L2, so time only, no HBM figure): the single boundary at
+    T = 4; the 49 decode MoE boundaries (layers 3..51, own weights, T = 128) as one graph; the
+    attention-side kernels at T = 128 and T = 2048."""
+    import residual_stream_norm_gb300 as rsn
+    L = rsn.lib()
+    out = {}
+    # config 1: single boundary, T = 4, n = 5
+    c = bi.boundary_case(T=4, n=5, seed=0)
+    h, x = c["h"].to(device), c["x"].to(device)
+    y = torch.empty_like(h)
+    wpo, wpr = c["w_post"].to(device), c["w_pre"].to(device)
+
+    def b4(st):
+        for _ in range(100):
+            assert L.beam_boundary_fwd(h.data_ptr(), y.data_ptr(), h.data_ptr(), x.data_ptr(),
+                                       wpo.data_ptr(), wpr.data_ptr(), 4, H, 5, bi.EPS, None,
+                                       st) == 0
+    us = graph_us(b4, 50, device) / 100
+    out["1_single_boundary_T4"] = {"us": round(us, 3), "tokens_per_s": round(4 / (us * 1e-6), 1),
+                                   "launches_per_graph": 100}
+    # config 3: decode MoE boundary, T = 128, layers 3..51 in one graph
+    m = bi.moe_case(T=128, seed=0)
+    hm, e, w = m["h"].to(device), m["e"].to(device), m["topk_w"].to(device)
+    ym = torch.empty_like(hm)
+    g = bi.rng(99)
+    layers = list(range(3, 52))
+    ws = [(bi.norm_weight(g, H).to(device), bi.norm_weight(g, H).to(device)) for _ in layers]
+
+    def moe49(st):
+        for (wa, wb), layer in zip(ws, layers):
+            assert L.beam_moe_combine_boundary_fwd(hm.data_ptr(), ym.data_ptr(), hm.data_ptr(),
+                                                   e.data_ptr(), w.data_ptr(), bi.ROUTED_SCALING,
+                                                   wa.data_ptr(), wb.data_ptr(), 128, H, K,
+                                                   2 * layer + 2, bi.EPS, None, st) == 0
+    us = graph_us(moe49, 50, device)
+    out["3_decode_moe_T128_layers_3_51"] = {
+        "us_per_launch": round(us / len(layers), 3), "us_per_49_launches": round(us, 2),
+        "tokens_per_s": round(128 * len(layers) / (us * 1e-6), 1)}
+    # config 4: attention side at T = 128 (positions U[0, 2^20)) and T = 2048 (contiguous)
+    for T, mode in ((128, "uniform"), (2048, "contiguous")):
+        a = bi.attn_qk_case(T=T, seed=T, pos_mode=mode)
+        q, k = a["q"].to(device), a["k"].to(device)
+        wq, wk, pos = a["wq"].to(device), a["wk"].to(device), a["pos"].to(device)
+        gc = bi.gate_case(T=T, seed=T + 1)
+        attn, gate, bias = gc["attn"].to(device), gc["gate"].to(device), gc["bias"].to(device)
+        go = torch.empty_like(attn)
+        row = {}
+        for name in ("qk_norm_rope", "qk_norm_ssmax", "attn_gate"):
+            def seq(st, name=name):
+                for _ in range(50):
+                    if name == "qk_norm_rope":
+                        r = L.beam_qk_norm_rope_fwd(q.data_ptr(), k.data_ptr(), NQ * D, NKV * D,
+                                                    wq.data_ptr(), wk.data_ptr(), pos.data_ptr(),
+                                                    T, NQ, NKV, D, bi.EPS, bi.ROPE_THETA, st)
+                    elif name == "qk_norm_ssmax":
+                        r = L.beam_qk_norm_ssmax_fwd(q.data_ptr(), k.data_ptr(), NQ * D, NKV * D,
+                                                     wq.data_ptr(), wk.data_ptr(),
+                                                     pos.data_ptr(), T, NQ, NKV, D, bi.EPS,
+                                                     bi.SSMAX_BASE, bi.SSMAX_EXP, st)
+                    else:
+                        r = L.beam_attn_gate_fwd(go.data_ptr(), attn.data_ptr(), gate.data_ptr(),
+                                                 bias.data_ptr(), T, NQ, D, NQ * D, NQ * D,
+                                                 NQ * D, st)
+                    assert r == 0
+            us = graph_us(seq, 20, device) / 50
+            row[name] = {"us": round(us, 3), "tokens_per_s": round(T / (us * 1e-6), 1)}
+        out[f"4_attention_T{T}"] = row
+    out["note"] = "CUDA graphs of back-to-back launches, warm; L2-resident: time only"
+    return out
+
+
+def oracle_per_config(host: dict, threads: int) -> dict:
+    """The oracle on each configuration of the workload, single-threaded and over token slices
+    on all host cores (where the configuration has more than one token): ms per launch (per
+    boundary for the decode chain) and tokens/s."""
+    import oracle
+    u = bi.u16
+
+    def timed(fn, min_s=0.2):
+        n, t0 = 0, time.perf_counter()
+        while True:
+            fn()
+            n += 1
+            el = time.perf_counter() - t0
+            if el >= min_s:
+                return el / n
+
+    def both(call, T, sample=None):
+        """call(lo, hi) over T tokens: single-threaded on `sample` tokens (scaled to T), and
+        token-parallel over all of them."""
+        ts = sample or T
+        one = timed(lambda: call(0, ts)) * T / ts
+        par = timed(lambda: oracle.run_token_parallel(call, T, threads)) if T > 1 else one
+        used = min(threads, T)
+        return {"ms_1core": round(one * 1e3, 3), "tokens_per_s_1core": round(T / one, 1),
+                f"ms_{used}cores": round(par * 1e3, 3), "tokens_per_s_ncores": round(T / par, 1),
+                "cores": used}
+
+    out = {}
+    c = bi.boundary_case(T=4, n=5, seed=0)
+    hu, xu, wa, wb = u(c["h"]), u(c["x"]), u(c["w_post"]), u(c["w_pre"])
+    out["1_single_boundary_T4"] = both(
+        lambda lo, hi: oracle.boundary(hu[lo:hi], xu[lo:hi], wa, wb, 5), 4)
+    ch = bi.decode_chain()
+    h0, xs, wpo, wpr = u(ch["h0"]), u(ch["xs"]), u(ch["w_post"]), u(ch["w_pre"])
+
+    def chain():
+        hh = h0
+        for i in range(bi.N_BOUNDARIES):
+            hh, _, _ = oracle.boundary(hh, xs[i], wpo[i], wpr[i], i + 1)
+    per = timed(chain) / bi.N_BOUNDARIES
+    out["2_decode_chain_T1"] = {"ms_per_boundary_1core": round(per * 1e3, 4), "cores": 1,
+                                "note": "one token: the chain is sequential"}
+    m = bi.moe_case(T=128, seed=0)
+    mh, me, mw, ma, mb = u(m["h"]), u(m["e"]), m["topk_w"].numpy(), u(m["w_post"]), u(m["w_pre"])
+    out["3_decode_moe_T128"] = both(
+        lambda lo, hi: oracle.moe_combine_boundary(mh[lo:hi], me[lo:hi], mw[lo:hi], ma, mb, 8),
+        128)
+    for T, mode in ((128, "uniform"), (2048, "contiguous")):
+        a = bi.attn_qk_case(T=T, seed=T, pos_mode=mode)
+        gc = bi.gate_case(T=T, seed=T + 1)
+        aq, ak, awq, awk, ap = u(a["q"]), u(a["k"]), u(a["wq"]), u(a["wk"]), a["pos"].numpy()
+        ga, gg, gb = u(gc["attn"]), u(gc["gate"]), gc["bias"].numpy()
+        out[f"4_attention_T{T}"] = {
+            "qk_norm_rope": both(lambda lo, hi: oracle.qk_norm_rope(aq[lo:hi], ak[lo:hi], awq,
+                                                                     awk, ap[lo:hi]), T),
+            "qk_norm_ssmax": both(lambda lo, hi: oracle.qk_norm_ssmax(aq[lo:hi], ak[lo:hi], awq,
+                                                                       awk, ap[lo:hi]), T),
+            "attn_gate": both(lambda lo, hi: oracle.attn_gate(ga[lo:hi], gg[lo:hi], gb, NQ, D),
+                              T)}
+    T = host["h"].shape[0]
+    hh, xx = u(host["h"]), u(host["x"])
+    w0, w1 = u(host["w_post"][0]), u(host["w_pre"][0])
+    he, ee, ew = u(host["h_m"]), u(host["e"]), host["topk_w"].numpy()
+    m0, m1 = u(host["w_post_m"]), u(host["w_pre_m"])
+    out["5_prefill_T16384"] = {
+        "boundary": both(lambda lo, hi: oracle.boundary(hh[lo:hi], xx[lo:hi], w0, w1, 1), T,
+                         sample=1024),
+        "moe_combine_boundary": both(
+            lambda lo, hi: oracle.moe_combine_boundary(he[lo:hi], ee[lo:hi], ew[lo:hi], m0, m1,
+                                                       2), T, sample=512),
+        "note": "single-threaded figures from a sample of the first 1024 (512) tokens, scaled"}
+    return out
+
+
+def next_rows(host: dict, device, peak: float, iters: int = ISOLATED_LAUNCHES) -> dict:
     """Rows beyond the five-kernel step at the step's T, each launch timed alone with CUDA
     events: the Q/K kernels fused with an FP8 KV-cache write (inputs larger than L2), and the
     grouped routing (16.8 MB of logits: L2-resident between launches, so its GB/s is not an
@@ -480,6 +763,88 @@ def next_rows(host: dict, device, peak: float, iters: int = 50) -> dict:
     return out
 
 
+E2E_SETS = 3        # device buffer sets in flight
+E2E_LANES = 2       # copy-in and copy-out streams each
+
+
+def end_to_end(step: "Step", host: dict, device, ws: int, args) -> dict:
+    """The step through host buffers: every step copies its inputs from pinned host memory,
+    runs the five kernels through the C ABI and copies its results back to pinned host memory.
+    Steps are pipelined the way a serving loop would run them: copy-in, compute and copy-out on
+    their own streams over E2E_SETS device buffer sets, each copy direction spread over
+    E2E_LANES streams (so that several copy engines can take part); events keep a buffer set
+    from being refilled before its results have left."""
+    e2e_steps = max(2 * E2E_SETS, min(args.steps, 12))
+    sets = [step] + [Step(host, device) for _ in range(E2E_SETS - 1)]
+    outs = [st_.outputs() for st_ in sets]
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs[0]]
+    h2d = sum(host[k].numel() * host[k].element_size() for k in INPUT_KEYS)
+    d2h = sum(o.numel() * o.element_size() for o in outs[0])
+    s_in = [torch.cuda.Stream(device) for _ in range(E2E_LANES)]
+    s_out = [torch.cuda.Stream(device) for _ in range(E2E_LANES)]
+    s_cmp = torch.cuda.Stream(device)
+    ev_in = [[torch.cuda.Event() for _ in range(E2E_LANES)] for _ in range(E2E_SETS)]
+    ev_out = [[torch.cuda.Event() for _ in range(E2E_LANES)] for _ in range(E2E_SETS)]
+    ev_cmp = [torch.cuda.Event() for _ in range(E2E_SETS)]
+    # inputs and outputs dealt to the lanes by size, largest first, to balance their bytes
+    def deal(items):
+        lanes, load = [[] for _ in range(E2E_LANES)], [0] * E2E_LANES
+        for key, nbytes in sorted(items, key=lambda kv: -kv[1]):
+            j = load.index(min(load))
+            lanes[j].append(key)
+            load[j] += nbytes
+        return lanes
+    in_lanes = deal([(k, host[k].numel() * host[k].element_size()) for k in INPUT_KEYS])
+    out_lanes = deal([(j, o.numel() * o.element_size()) for j, o in enumerate(outs[0])])
+    torch.cuda.synchronize(device)
+    barrier(ws)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s_ in s_in + s_out + [s_cmp]:
+        s_.wait_event(e0)
+    for i in range(e2e_steps):
+        b = i % E2E_SETS
+        for lane in range(E2E_LANES):
+            st = s_in[lane]
+            if i >= E2E_SETS:
+                for ev in ev_out[b]:
+                    st.wait_event(ev)  # this set's previous results have left
+            with torch.cuda.stream(st):
+                for k in in_lanes[lane]:
+                    sets[b].dev[k].copy_(host[k], non_blocking=True)
+            ev_in[b][lane].record(st)
+        for ev in ev_in[b]:
+            s_cmp.wait_event(ev)
+        with torch.cuda.stream(s_cmp):
+            sets[b].launch(i)
+        ev_cmp[b].record(s_cmp)
+        for lane in range(E2E_LANES):
+            st = s_out[lane]
+            st.wait_event(ev_cmp[b])
+            with torch.cuda.stream(st):
+                for j in out_lanes[lane]:
+                    host_out[j].copy_(outs[b][j], non_blocking=True)
+            ev_out[b][lane].record(st)
+    cur = torch.cuda.current_stream(device)
+    for s_ in s_in + s_out + [s_cmp]:
+        cur.wait_stream(s_)
+    e1.record()
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
+    T = step.T
+    e2e = {"value": round(ws * T * e2e_steps / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "path": f"pinned host buffers -> cudaMemcpyAsync -> C ABI -> cudaMemcpyAsync -> host; "
+                   f"copy-in ({E2E_LANES} streams), compute and copy-out ({E2E_LANES} streams) "
+                   f"pipelined over {E2E_SETS} buffer sets; the host link bounds it (host_link: "
+                   f"each direction's copy bandwidth measured in this run, and the bytes/s the "
+                   f"pipelined run moved both ways)"}
+    del sets[1:]
+    e2e["host_link"] = host_link(device)
+    e2e["host_link"]["e2e_gb_s"] = round((h2d + d2h) * e2e_steps / (e2e_ms * 1e-3) / 1e9, 1)
+    return e2e
+
+
 def run_gpu_arm(args) -> None:
     ws, rank, local = dist_env()
     device = torch.device("cuda", local)
@@ -492,7 +857,6 @@ def run_gpu_arm(args) -> None:
     step = Step(host, device)
     torch.cuda.synchronize(device)
 
-    launches_per_step = 5
     for i in range(args.warmup):
         step.launch(i)
     torch.cuda.synchronize(device)
@@ -511,7 +875,6 @@ def run_gpu_arm(args) -> None:
     torch.cuda.synchronize(device)
     t_wall1 = time.perf_counter()
     barrier(ws)
-    clocks.stop()
 
     total_ms = ev[0][0].elapsed_time(ev[-1][nk])
     per_kernel_ms = {KERNELS[j]: sum(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(args.steps))
@@ -521,77 +884,39 @@ def run_gpu_arm(args) -> None:
     value = whole_job_rate(ws, T, args.steps, max_ms)
 
     peak, peak_src = measured_peak()
-    kernels = {}
+    # per kernel, in the step: the launches of the timed region (CUDA events between launches)
+    in_step = {}
     for name in KERNELS:
-        ms = per_kernel_ms[name]
-        by = BYTES_PER_TOKEN[name] * T
-        gbs = by / (ms * 1e-3) / 1e9
-        kernels[name] = {"us": round(ms * 1e3, 2), "bytes_per_launch": by,
-                         "gb_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
-                         "tokens_per_s": round(T / (ms * 1e-3), 1),
-                         "share": round(ms / sum(per_kernel_ms.values()), 4)}
+        in_step[name] = kernel_row(name, per_kernel_ms[name], BYTES_PER_TOKEN[name], T, peak)
+        in_step[name]["share"] = round(per_kernel_ms[name] / sum(per_kernel_ms.values()), 4)
     dom = max(KERNELS, key=lambda k: per_kernel_ms[k])
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": in_step[dom]["gb_s"],
+                "peak": peak, "unit": "GB/s", "frac": in_step[dom]["frac_of_peak"],
+                "traffic": None, "peak_source": peak_src,
+                "algorithmic_bytes_per_launch": in_step[dom]["bytes_per_launch"],
+                "launches_timed": args.steps,
+                "how": "algorithmic bytes / mean launch time of the kernel over the timed "
+                       "region (CUDA events on the launching stream)"}
     tr = profiled_traffic(dom, T)
-    roofline = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom]["gb_s"],
-                "peak": peak, "unit": "GB/s", "frac": kernels[dom]["frac_of_peak"],
-                "traffic": tr, "peak_source": peak_src,
-                "algorithmic_bytes_per_launch": kernels[dom]["bytes_per_launch"]}
+    if tr:
+        roofline.update(tr)
 
-    # end to end: every step copies its inputs from pinned host memory, runs the five kernels
-    # through the C ABI and copies its results back to pinned host memory.  Steps are pipelined
-    # the way a serving loop would run them: three streams (copy in, compute, copy out) and two
-    # device buffer sets, so that step i+1's inputs travel while step i computes and step i-1's
-    # results come back; events keep a buffer set from being refilled before its results left.
-    e2e_steps = min(args.steps, 10)
-    sets = [step, Step(host, device)]
-    outs = [st_.outputs() for st_ in sets]
-    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs[0]]
-    h2d = sum(host[k].numel() * host[k].element_size() for k in INPUT_KEYS)
-    d2h = sum(o.numel() * o.element_size() for o in outs[0])
-    s_in, s_cmp, s_out = (torch.cuda.Stream(device) for _ in range(3))
-    ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "cmp", "out")}
-    torch.cuda.synchronize(device)
-    barrier(ws)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for s_ in (s_in, s_cmp, s_out):
-        s_.wait_event(e0)
-    for i in range(e2e_steps):
-        b = i & 1
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(ev["out"][b])  # this set's previous results have left
-            for k in INPUT_KEYS:
-                sets[b].dev[k].copy_(host[k], non_blocking=True)
-            ev["in"][b].record(s_in)
-        with torch.cuda.stream(s_cmp):
-            s_cmp.wait_event(ev["in"][b])
-            sets[b].launch(i)
-            ev["cmp"][b].record(s_cmp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev["cmp"][b])
-            for o, ho in zip(outs[b], host_out):
-                ho.copy_(o, non_blocking=True)
-            ev["out"][b].record(s_out)
-    cur = torch.cuda.current_stream(device)
-    for s_ in (s_in, s_cmp, s_out):
-        cur.wait_stream(s_)
-    e1.record()
-    torch.cuda.synchronize(device)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
-    e2e = {"value": round(ws * T * e2e_steps / (e2e_ms * 1e-3), 1), "unit": "tokens/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-           "path": "pinned host buffers -> cudaMemcpyAsync -> C ABI -> cudaMemcpyAsync -> host; "
-                   "copy-in, compute and copy-out streams pipelined over two buffer sets; the "
-                   "host link bounds it (host_link: each direction's copy bandwidth measured "
-                   "in this run, and the bytes/s the pipelined run moved both ways)"}
-    del sets[1]
-    e2e["host_link"] = host_link(device)
-    # bytes that cross the host link per second of the pipelined run, both ways together
-    e2e["host_link"]["e2e_gb_s"] = round((h2d + d2h) * e2e_steps / (e2e_ms * 1e-3) / 1e9, 1)
+    # per kernel, alone: ISOLATED_LAUNCHES launches of its own (independent of --steps)
+    t_iso0 = time.perf_counter()
+    kernels = isolated_kernels(step, device, peak)
+    for name in KERNELS:
+        kernels[name]["share_in_step"] = in_step[name]["share"]
+    roofline["isolated"] = {"us": kernels[dom]["us"], "gb_s": kernels[dom]["gb_s"],
+                            "frac": kernels[dom]["frac_of_peak"],
+                            "launches": ISOLATED_LAUNCHES}
 
+    e2e = end_to_end(step, host, device, ws, args)
     decode = decode_chain_us(device)
     nxt = next_rows(host, device, peak)
+    nxt["allreduce_boundary_tp8"] = allreduce_rows(device, peak)
+    small = small_configs(device)
+    t_iso1 = time.perf_counter()
+    clocks.stop()
     ceiling = copy_ceiling(device)
     roofline["copy_ceiling_gbs"] = ceiling["gb_s"]
     roofline["frac_of_copy_ceiling"] = round(roofline["achieved"] / ceiling["gb_s"], 4)
@@ -605,26 +930,30 @@ def run_gpu_arm(args) -> None:
         cpu = {"value": round(T / cpu_s, 1), "unit": "tokens/s", "cores": threads,
                "kind": "oracle",
                "sample": f"one full step ({T} tokens through all five operations), "
-                         f"{threads} threads over token slices, {cpu_s:.2f} s wall"}
+                         f"{threads} threads over token slices, {cpu_s:.2f} s wall",
+               "per_config": oracle_per_config(host, threads)}
+        b = kernels["boundary"]
         out = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(max_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage": "bf16",
             "data": "synthetic (seeded, Beam-shaped)",
-            "config": {"workload": "prefill 8x2048 = 16384 tokens at ~100K context: one pass of "
-                                   "qk_norm_rope, qk_norm_ssmax, attn_gate, boundary, "
-                                   "moe_combine_boundary (hidden 5120, 48/8 heads x 128, top-8)",
-                       "tokens_per_step": T, "hidden": H, "top_k": K,
-                       "l2": "inputs larger than L2 (every kernel streams >= 168 MB per launch; "
-                             "L2 129 MB); no flush",
-                       "parallelism": f"replicas x{ws}"},
-            "kernels": kernels, "roofline": roofline, "copy_ceiling": ceiling,
-            "decode": decode, "next": nxt,
+            "config": bench_config(ws),
+            "value_is": "tokens/s of the whole step (all five kernels over the same 16384 tokens)",
+            "boundary_T16384": {"tokens_per_s": b["tokens_per_s"], "gb_s": b["gb_s"],
+                                "frac_of_peak": b["frac_of_peak"], "us": b["us"],
+                                "launches": ISOLATED_LAUNCHES},
+            "decode_us_per_boundary": decode["us_per_boundary"],
+            "kernels": kernels, "kernels_in_step": in_step, "roofline": roofline,
+            "copy_ceiling": ceiling,
+            "decode": decode, "configs": small, "next": nxt,
             "e2e": e2e,
             "cpu_baseline": cpu, "gpu_launches": gpu_launches * ws,
             "clocks": clocks.summary(t_wall0, t_wall1),
+            "clocks_whole_run": clocks.summary(t_wall0, t_iso1),
             "wall_timed_s": round(t_wall1 - t_wall0, 4),
+            "wall_isolated_s": round(t_iso1 - t_iso0, 2),
         }
     if ws > 1:
         torch.distributed.barrier()
@@ -658,10 +987,7 @@ def run_reference_arm(args) -> None:
         "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "storage": "bf16",
         "data": "synthetic (seeded, Beam-shaped)",
-        "config": {"workload": "prefill 8x2048 = 16384 tokens at ~100K context: one pass of "
-                               "qk_norm_rope, qk_norm_ssmax, attn_gate, boundary, "
-                               "moe_combine_boundary (hidden 5120, 48/8 heads x 128, top-8)",
-                   "tokens_per_step": T, "hidden": H, "top_k": K},
+        "config": bench_config(ws),
         "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{per_step} of the {T} tokens per step, all five operations"},

@@ -2,8 +2,8 @@
 
     python -m residual_stream_norm_gb300.profile_case --kernel moe --tokens 2048 --launches 3
 
-Kernels: boundary, moe, qk_rope, qk_ssmax, gate, qk_rope_kv and qk_ssmax_kv (FP8 KV cache),
-routing.  Inputs come from the seeded generators; the case is sized by --tokens (2048 tokens keep
+Kernels: boundary, moe, allreduce (TP8 partials), qk_rope, qk_ssmax, gate, qk_rope_kv and
+qk_ssmax_kv (FP8 KV cache), routing.  Inputs come from the seeded generators; the case is sized by --tokens (2048 tokens keep
 every kernel's inputs above the 129 MB L2 for the MoE variant and a few hundred MB on the device
 at most).
 """
@@ -24,7 +24,7 @@ import residual_stream_norm_gb300 as rsn  # noqa: E402
 def main(argv=None) -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--kernel", required=True,
-                    choices=["boundary", "moe", "qk_rope", "qk_ssmax", "gate", "qk_rope_kv",
+                    choices=["boundary", "moe", "allreduce", "qk_rope", "qk_ssmax", "gate", "qk_rope_kv",
                              "qk_ssmax_kv", "routing"])
     ap.add_argument("--tokens", type=int, default=2048)
     ap.add_argument("--launches", type=int, default=3)
@@ -44,6 +44,12 @@ def main(argv=None) -> None:
         wpo, wpr = c["w_post"].to(dev), c["w_pre"].to(dev)
         y = torch.empty_like(h)
         run = lambda i: rsn.beam_moe_combine_boundary_fwd(h, y, h, e, w, wpo, wpr, 2 * (i % 52) + 2)
+    elif args.kernel == "allreduce":
+        c = bi.allreduce_case(T=T, P=bi.TP_RANKS)
+        h, parts = c["h"].to(dev), c["parts"].to(dev)
+        wpo, wpr = c["w_post"].to(dev), c["w_pre"].to(dev)
+        y = torch.empty_like(h)
+        run = lambda i: rsn.beam_allreduce_boundary_fwd(h, y, h, parts, wpo, wpr, i % 104 + 1)
     elif args.kernel in ("qk_rope", "qk_ssmax"):
         c = bi.attn_qk_case(T=T, pos_mode="uniform" if args.kernel == "qk_rope" else "contiguous")
         q, k = c["q"].to(dev), c["k"].to(dev)
