@@ -125,13 +125,21 @@ __device__ __forceinline__ void cache_store(void *cache, int64_t e, uint4 o, int
 // masked to its quad.
 
 // The per-token factors of one tile: 64 cos/sin pairs per token (RoPE), or the SSMax query
-// scale.  cos/sin are the FP32 roundings of the exact values of the FP32 angle.
-template <bool ROPE, int TT>
+// scale, and with a KV cache the tokens' cache slots.  cos/sin are the FP32 roundings of the exact
+// values of the FP32 angle.
+template <bool ROPE, bool KV, int TT>
 __device__ __forceinline__ void tile_factors(const QkArgs &a, const RopeTable &tab, int64_t t0,
                                              int nt, float (&cs)[TT][kHalf],
-                                             float (&sn)[TT][kHalf], float (&scale_q)[TT])
+                                             float (&sn)[TT][kHalf], float (&scale_q)[TT],
+                                             int64_t (&slot)[TT])
 {
     const int tid = threadIdx.x;
+    if (KV && tid >= blockDim.x - TT && tid - (int)(blockDim.x - TT) < nt) {
+        // the tokens' cache slots (-1: padding or out of range), by the last threads
+        const int tt = tid - (int)(blockDim.x - TT);
+        const int64_t s = a.slot[t0 + tt];
+        slot[tt] = s >= 0 && s < a.num_slots ? s : -1;
+    }
     if constexpr (ROPE) {
         for (int i = tid; i < nt * kHalf; i += blockDim.x) {
             const int tt = i / kHalf, f = i - tt * kHalf;
@@ -156,24 +164,21 @@ __device__ __forceinline__ void tile_factors(const QkArgs &a, const RopeTable &t
 
 // One item: normalise, rotate / scale, round, store (and write the KV cache).  `v` holds the
 // lane's four vectors (see above), `row` the item's row in global memory (nullptr: an inactive
-// item, whose lanes still take part in every shuffle), `tt` / `hd` its token within the tile and
-// its head (Q heads, then K, then V), `cst` / `snt` / `sq` the token's factors.  All lanes of the
+// item, whose lanes still take part in every shuffle), `hd` its head (Q heads, then K, then V),
+// `tslot` its token's cache slot, `cst` / `snt` / `sq` the token's factors.  All lanes of the
 // warp call it together.
 template <bool ROPE, bool KV>
-__device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], char *row, int tt,
-                                        int hd, int64_t t0, int q, unsigned qmask,
+__device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], char *row, int hd,
+                                        int64_t tslot, int q, unsigned qmask,
                                         const float (&wsm)[2][kHeadDim], const float *cst,
                                         const float *snt, float sq, f2 nz)
 {
     const int nqk = a.n_q + a.n_kv;
     const bool act = row != nullptr;  // uniform across each quad
     const bool isq = hd < a.n_q;
-    // the cache slot of a K or V item (-1: no cache, padding or out of range)
-    int64_t cslot = -1;
-    if (KV && act && !isq) {
-        const int64_t s = a.slot[t0 + tt];
-        cslot = s >= 0 && s < a.num_slots ? s : -1;
-    }
+    // the cache slot of a K or V item (-1: no cache, padding or out of range); tslot is the
+    // token's slot, checked against the cache when the tile's factors were formed
+    const int64_t cslot = KV && act && !isq ? tslot : -1;
     if (KV && hd >= nqk) {  // a V item: into the V cache, unchanged
         if (cslot >= 0) {
             const int64_t e0 = (cslot * a.n_kv + (hd - nqk)) * kHeadDim;
@@ -196,20 +201,24 @@ __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], ch
         // ulp: the head sum is rounded as the exact sum would be.
         // Each of the two packed accumulators starts from M, the largest square of the lane,
         // so that its running sum is never below the next term and Dekker's Fast2Sum (3 adds)
-        // is exact in place of TwoSum (6); 2M is taken off after the lanes are merged.
-        float mabs = 0.0f;
+        // is exact in place of TwoSum (6); 2M is taken off after the lanes are merged.  The
+        // lane's largest |x| comes from an integer maximum of the BF16 magnitude bits (which
+        // order like the magnitudes; a NaN element gives a NaN M, and the sum then takes the
+        // exact path below, as an infinite one does), off the FP32 pipe.
+        uint32_t mw = 0u;
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp)
-                mabs = fmaxf(mabs, fmaxf(fabsf(lo_of(x[jj][pp])), fabsf(hi_of(x[jj][pp]))));
+                mw = max_u16x2(mw, word(v[jj], pp) & 0x7fff7fffu);
+        const float mabs = __uint_as_float(max(mw & 0xffffu, mw >> 16) << 16);
         const float m2 = __fmul_rn(mabs, mabs);  // exact: the square of a BF16 value
         Sum2x2 acc = {splat(m2), 0ull};
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj)
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp)
-                fast2_add(acc, mul2(x[jj][pp], x[jj][pp]));
+                fast2_add_sq(acc, x[jj][pp]);
         Sum2 tot = sum_merge(Sum2{lo_of(acc.hi), lo_of(acc.lo)}, Sum2{hi_of(acc.hi), hi_of(acc.lo)});
         tot = sum_merge(tot, Sum2{-__fadd_rn(m2, m2), 0.0f});
 #pragma unroll
@@ -305,6 +314,24 @@ __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], ch
     }
 }
 
+// m = ceil(2^32 / n), in 64 bits (2^32 itself for n = 1): with e = m n - 2^32 < n,
+// floor(j m / 2^32) = floor(j / n) whenever j e < 2^32 -- for every j < 2^14 when n < 2^12 (here
+// n <= 2048 heads, j < 8 n).
+__device__ __forceinline__ uint64_t div_magic(int n)
+{
+    return ((1ull << 32) + (uint64_t)n - 1) / (uint64_t)n;
+}
+
+// Token tt and head hd of item j of a tile of items (token-major, nheads heads a token);
+// inactive items (j >= nitems) map to (0, 0).
+__device__ __forceinline__ void item_of(int j, int nitems, int nheads, uint64_t hmag, int &tt,
+                                        int &hd)
+{
+    const uint32_t jj = j < nitems ? (uint32_t)j : 0u;
+    tt = (int)(((uint64_t)jj * hmag) >> 32);
+    hd = (int)jj - tt * nheads;
+}
+
 // Global row of item (token t, head hd): Q heads, then K, then V.
 __device__ __forceinline__ char *item_row(const QkArgs &a, int64_t t, int hd, int nqk)
 {
@@ -325,9 +352,11 @@ __global__ void __launch_bounds__(kQkThreads, 4) qk_norm_kernel(const QkArgs a, 
     __shared__ __align__(16) float cs[2][TT][kHalf];  // double-buffered by tile parity
     __shared__ __align__(16) float sn[2][TT][kHalf];
     __shared__ float scale_q[2][TT];
+    __shared__ int64_t tslot[2][TT];
     __shared__ __align__(16) float wsm[2][kHeadDim];  // wq, wk as FP32
     const int nqk = a.n_q + a.n_kv;
     const int nheads = nqk + (KV ? a.n_kv : 0);  // Q, K, then V heads
+    const uint64_t hmag = div_magic(nheads);
     // shuffles: masked to the quad when V items may send quads of a warp different ways,
     // warp-wide otherwise
     const unsigned qmask = KV ? 0xfu << (threadIdx.x & 28) : 0xffffffffu;
@@ -360,11 +389,8 @@ __global__ void __launch_bounds__(kQkThreads, 4) qk_norm_kernel(const QkArgs a, 
 #pragma unroll
             for (int m = 0; m < kIPP; ++m) {
                 const int j = base + slot + kSlots * m;
-                int tt = 0, hd = j < nitems ? j : 0;  // inactive items map to (0, 0)
-                while (hd >= nheads) {  // at most TT - 1 steps
-                    hd -= nheads;
-                    ++tt;
-                }
+                int tt, hd;
+                item_of(j, nitems, nheads, hmag, tt, hd);
                 tok[m] = tt;
                 head[m] = hd;
                 row[m] = j < nitems ? item_row(a, t0 + tt, hd, nqk) : nullptr;
@@ -374,13 +400,14 @@ __global__ void __launch_bounds__(kQkThreads, 4) qk_norm_kernel(const QkArgs a, 
             }
             // ---- per-token factors of the tile, once, while the first loads fly -------------
             if (base == 0) {
-                tile_factors<ROPE, TT>(a, tab, t0, nt, cs[buf], sn[buf], scale_q[buf]);
+                tile_factors<ROPE, KV, TT>(a, tab, t0, nt, cs[buf], sn[buf], scale_q[buf],
+                                           tslot[buf]);
                 __syncthreads();
             }
 #pragma unroll
             for (int m = 0; m < kIPP; ++m)
-                qk_item<ROPE, KV>(a, v[m], row[m], tok[m], head[m], t0, q, qmask, wsm,
-                                  cs[buf][tok[m]], sn[buf][tok[m]],
+                qk_item<ROPE, KV>(a, v[m], row[m], head[m], KV ? tslot[buf][tok[m]] : -1, q,
+                                  qmask, wsm, cs[buf][tok[m]], sn[buf][tok[m]],
                                   ROPE ? 0.0f : scale_q[buf][tok[m]], splat(tab.neg_zero));
         }
     }
@@ -404,16 +431,21 @@ __device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wai
 // A thread reads back only what it copied itself, so no barrier guards the staging buffers;
 // [pass parity][vector][thread] keeps a warp's reads of one vector contiguous (no bank
 // conflicts).
+// 4 CTAs of 8 warps on an SM (64 registers) without a KV cache; with one, 3 CTAs (85 registers):
+// at 64 its V path and cache stores spilled, and it took 110.6 us against 104.8 us at T = 16384.
 template <bool ROPE, int TT, bool KV>
-__global__ void __launch_bounds__(kQkThreads, 4) qk_stage_kernel(const QkArgs a, const RopeTable tab)
+__global__ void __launch_bounds__(kQkThreads, KV ? 3 : 4)
+    qk_stage_kernel(const QkArgs a, const RopeTable tab)
 {
     __shared__ __align__(16) float cs[2][TT][kHalf];  // double-buffered by tile parity
     __shared__ __align__(16) float sn[2][TT][kHalf];
     __shared__ float scale_q[2][TT];
+    __shared__ int64_t tslot[2][TT];
     __shared__ __align__(16) float wsm[2][kHeadDim];
     __shared__ __align__(16) uint4 stage[2][4][kQkThreads];
     const int nqk = a.n_q + a.n_kv;
     const int nheads = nqk + (KV ? a.n_kv : 0);
+    const uint64_t hmag = div_magic(nheads);
     const unsigned qmask = KV ? 0xfu << (threadIdx.x & 28) : 0xffffffffu;
     const int tid = threadIdx.x;
     const int q = tid & 3;
@@ -439,12 +471,7 @@ __global__ void __launch_bounds__(kQkThreads, 4) qk_stage_kernel(const QkArgs a,
         // item of pass p for this quad: token tt and head hd of the tile, or none
         auto locate = [&](int p, int &tt, int &hd) -> char * {
             const int j = p * kSlots + slot;
-            tt = 0;
-            hd = j < nitems ? j : 0;
-            while (hd >= nheads) {
-                hd -= nheads;
-                ++tt;
-            }
+            item_of(j, nitems, nheads, hmag, tt, hd);
             return j < nitems ? item_row(a, t0 + tt, hd, nqk) : nullptr;
         };
         auto issue = [&](int p) {
@@ -463,7 +490,8 @@ __global__ void __launch_bounds__(kQkThreads, 4) qk_stage_kernel(const QkArgs a,
             else
                 cp_async_commit();  // an empty group keeps "all but the newest" meaning pass p
             if (p == 0) {  // the tile's factors, while the first copies fly
-                tile_factors<ROPE, TT>(a, tab, t0, nt, cs[buf], sn[buf], scale_q[buf]);
+                tile_factors<ROPE, KV, TT>(a, tab, t0, nt, cs[buf], sn[buf], scale_q[buf],
+                                           tslot[buf]);
                 __syncthreads();
             }
             cp_async_wait_one();
@@ -473,8 +501,9 @@ __global__ void __launch_bounds__(kQkThreads, 4) qk_stage_kernel(const QkArgs a,
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
                 v[jj] = row ? stage[p & 1][jj][tid] : zero;
-            qk_item<ROPE, KV>(a, v, row, tt, hd, t0, q, qmask, wsm, cs[buf][tt], sn[buf][tt],
-                              ROPE ? 0.0f : scale_q[buf][tt], splat(tab.neg_zero));
+            qk_item<ROPE, KV>(a, v, row, hd, KV ? tslot[buf][tt] : -1, q, qmask, wsm,
+                              cs[buf][tt], sn[buf][tt], ROPE ? 0.0f : scale_q[buf][tt],
+                              splat(tab.neg_zero));
         }
     }
 }
@@ -556,12 +585,16 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
     for (int i = 0; i < kHalf; ++i)
         tab.inv_freq[i] = ROPE ? a.inv_freq_host[i] : 0.0f;
     tab.neg_zero = -0.0f;
-    const bool many = a.T >= 4 * (int64_t)device_sm_count();
+    const int64_t sms = device_sm_count();
     // Many tokens: 4 CTAs of 8 warps on an SM, one head per quad per pass, tiles of 8 tokens for
     // RoPE (each thread then forms two cos/sin pairs per tile) and 4 for SSMax.  The staged
     // kernel keeps a second pass's reads in flight; it pays off where a head costs the most
     // arithmetic (RoPE) or the V rows add reads (the KV cache), while plain SSMax is as fast
-    // without it.  Few tokens: one token per CTA spreads them over more SMs.
+    // without it.  Fewer tokens: one token per CTA spreads them over more SMs.  The staged
+    // kernel's 8-token tiles need many tokens to fill the GPU: RoPE took 25.4 us at T = 2048 and
+    // 31-33 us at T = 4096 with them, against 14.1 and 27.4 us with one-token tiles (and 82 us
+    // against 104 us at T = 16384), so it starts at 32 tokens per SM.
+    const bool many = a.T >= (ROPE || KV ? 32 : 4) * sms;
     constexpr int TT = ROPE ? 8 : 4;
     const dim3 block(kQkThreads);
     cudaError_t e;

@@ -338,11 +338,12 @@ int beam_allreduce_boundary_fwd(void *h_out, void *y_out, const void *h_in,
         if (!aligned(x_parts[p], 16))
             return BEAM_ERR_MISALIGNED;
     beam::BoundaryArgs a = boundary_args();
+    beam::TpParts parts{};
     a.h_out = h_out;
     a.y_out = y_out;
     a.h_in = h_in;
     for (int32_t p = 0; p < P; ++p)
-        a.parts[p] = x_parts[p];
+        parts.p[p] = x_parts[p];
     a.P = P;
     a.w_post = w_post;
     a.w_pre = w_pre;
@@ -352,7 +353,7 @@ int beam_allreduce_boundary_fwd(void *h_out, void *y_out, const void *h_in,
     a.eps = eps;
     beam_residual_scales(n, &a.alpha, &a.s);
     set_residual_rule(a);
-    return cuda_status(beam::launch_allreduce_boundary(a, stream));
+    return cuda_status(beam::launch_allreduce_boundary(a, parts, stream));
 }
 
 int beam_selftest_persistent_timeout(int32_t kind, void *h_out, void *y_out, float *rstd_out,

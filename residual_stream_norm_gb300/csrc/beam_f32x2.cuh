@@ -152,11 +152,14 @@ __device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b)
     return d;
 }
 
-// Packed compensated sum: two independent Knuth TwoSum accumulators, one per lane.
+// Packed compensated sum: two independent accumulators (hi, lo), one per lane.
 struct Sum2x2 {
     f2 hi, lo;
 };
 
+// Adds t >= 0 to an accumulator with Knuth's TwoSum (an error-free transformation: the new
+// hi + the new error term is exactly hi + t), the error added to lo.  (Folding a square t = x x
+// into FMAs here measured 2% slower in the MoE ring.)
 __device__ __forceinline__ void sum2_add(Sum2x2 &a, f2 t)
 {
     const f2 s = add2(a.hi, t);
@@ -167,12 +170,14 @@ __device__ __forceinline__ void sum2_add(Sum2x2 &a, f2 t)
     a.lo = add2(a.lo, e);
 }
 
-// Adds t >= 0 to an accumulator whose running sum is at least t (both lanes): Dekker's Fast2Sum,
-// exact under that condition.
-__device__ __forceinline__ void fast2_add(Sum2x2 &a, f2 t)
+// Adds t = x x (exact) to an accumulator whose running sum is at least t (both lanes) with
+// Dekker's Fast2Sum (s = hi + t; error t - (s - hi), exact under that condition), the square
+// folded into two FMAs: s = RN(x x + hi), and the error RN(x x + (hi - s)), where hi - s is the
+// exact, negated s - hi of Fast2Sum.
+__device__ __forceinline__ void fast2_add_sq(Sum2x2 &a, f2 x)
 {
-    const f2 s = add2(a.hi, t);
-    const f2 e = sub2(t, sub2(s, a.hi));
+    const f2 s = fma2(x, x, a.hi);
+    const f2 e = fma2(x, x, sub2(a.hi, s));
     a.hi = s;
     a.lo = add2(a.lo, e);
 }
@@ -185,6 +190,14 @@ __device__ __forceinline__ Sum2x2 sum2_merge(const Sum2x2 &a, const Sum2x2 &b)
     const f2 ap = sub2(s, bp);
     const f2 e = add2(sub2(a.hi, ap), sub2(b.hi, bp));
     return Sum2x2{s, add2(add2(a.lo, b.lo), e)};
+}
+
+// Lane-wise unsigned maximum of two pairs of 16-bit values.
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 // Bit 15 of each 16-bit half stays set only if that BF16 element of `w` has an exponent field

@@ -35,7 +35,6 @@ struct BoundaryArgs {
     const void *x_in;        // boundary: sublayer output [T, H]
     const void *expert_out;  // MoE: [T, K, H] (x_in unused)
     const float *topk_w;     // MoE: [T, K]
-    const void *parts[kMaxParts];  // tensor parallel: P partial sublayer outputs [T, H] each
     const void *w_post;
     const void *w_pre;
     float *rstd_out;         // [T, 2] or nullptr
@@ -51,6 +50,12 @@ struct BoundaryArgs {
     uint32_t floor_bits;     // (f << 7) | (f << 23), f = residual_floor_exp(s)
     float eps;
     unsigned long long wait_ns;  // limit of a persistent kernel's wait on its own copies
+};
+
+// The tensor-parallel partials of the all-reduce boundary, a kernel parameter of its own so
+// that the other boundary kernels' parameters stay small (they are copied at every launch).
+struct TpParts {
+    const void *p[kMaxParts];  // P partial sublayer outputs [T, H] each
 };
 
 struct QkArgs {
@@ -107,7 +112,8 @@ struct GateArgs {
 
 cudaError_t launch_boundary(const BoundaryArgs &a, cudaStream_t stream);
 cudaError_t launch_moe_boundary(const BoundaryArgs &a, cudaStream_t stream);
-cudaError_t launch_allreduce_boundary(const BoundaryArgs &a, cudaStream_t stream);
+cudaError_t launch_allreduce_boundary(const BoundaryArgs &a, const TpParts &parts,
+                                      cudaStream_t stream);
 // Runs a persistent boundary kernel (moe: the MoE ring with K slots, else the plain boundary's
 // prefetch kernel) with its bulk copies withheld: its first wait runs out after a.wait_ns, it
 // raises the fault word and writes nothing.  a.K is the MoE slot count; inputs are not read.

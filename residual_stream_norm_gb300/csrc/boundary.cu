@@ -39,6 +39,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <type_traits>
 
 #include "beam_device.cuh"
 #include "beam_exact.cuh"
@@ -62,6 +63,16 @@ struct ExactSlot {
     uint32_t sticky, max_bits;
 };
 
+// Barrier of the threads that share a row: the whole CTA (bar 0), or the `nt` threads of named
+// barrier `bar` (a row group of a multi-group CTA, or the ring's consumer warps).
+__device__ __forceinline__ void group_sync(int bar, int nt)
+{
+    if (bar == 0)
+        __syncthreads();
+    else
+        named_sync(bar, nt);
+}
+
 // A thread's VPT packed BF16 vectors, copied for the rare exact path.
 template <int VPT>
 struct Vecs {
@@ -75,7 +86,7 @@ struct Vecs {
 // code and few registers.
 template <int VPT>
 __device__ __forceinline__ float block_sum_exact(const Vecs<VPT> vv, ExactSlot *xslot, int nt,
-                                              bool named)
+                                                 int wbase, int bar)
 {
     const uint4 (&v)[VPT] = vv.v;
     const int lane = threadIdx.x & 31;
@@ -94,12 +105,9 @@ __device__ __forceinline__ float block_sum_exact(const Vecs<VPT> vv, ExactSlot *
     mx = __reduce_max_sync(0xffffffffu, mx);
     if (lane == 0)
         xslot[warp].max_bits = mx;
-    if (named)
-        named_sync(1, nt);
-    else
-        __syncthreads();
+    group_sync(bar, nt);
     for (int w = 0; w < nw; ++w)
-        mx = max(mx, xslot[w].max_bits);
+        mx = max(mx, xslot[wbase + w].max_bits);
     if (mx >= 0x7f800000u)  // a NaN or infinite square: the IEEE sum
         return __uint_as_float(mx > 0x7f800000u ? 0x7fc00000u : 0x7f800000u);
     if (mx == 0u)
@@ -127,13 +135,10 @@ __device__ __forceinline__ float block_sum_exact(const Vecs<VPT> vv, ExactSlot *
         xslot[warp].lo = acc.lo;
         xslot[warp].sticky = acc.sticky;
     }
-    if (named)
-        named_sync(1, nt);
-    else
-        __syncthreads();
+    group_sync(bar, nt);
     ExactAcc t = {0ull, 0ull, 0u};
     for (int w = 0; w < nw; ++w)
-        exact_merge(t, ExactAcc{xslot[w].hi, xslot[w].lo, xslot[w].sticky});
+        exact_merge(t, ExactAcc{xslot[wbase + w].hi, xslot[wbase + w].lo, xslot[wbase + w].sticky});
     return exact_round(t, emax);
 }
 
@@ -148,7 +153,7 @@ __device__ __forceinline__ Sum2x2 squares_sum(const uint4 (&v)[VPT])
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const f2 x = widen(word(v[i], j));
-            sum2_add(acc[j], mul2(x, x));
+            sum2_add(acc[j], mul2(x, x));  // x x is exact: the square of a BF16 value
         }
     return sum2_merge(sum2_merge(acc[0], acc[1]), sum2_merge(acc[2], acc[3]));
 }
@@ -158,26 +163,24 @@ __device__ __forceinline__ Sum2 lanes_merged(const Sum2x2 &a)
     return sum_merge(Sum2{lo_of(a.hi), lo_of(a.lo)}, Sum2{hi_of(a.hi), hi_of(a.lo)});
 }
 
-// Block-wide sum over `nt` threads (a multiple of 32) of the squares of their vectors `v`, of
-// which each thread has formed the compensated partial sum `acc`; rounded as the exact sum would
-// be.  `named`: synchronise only those threads on named barrier 1 (the ring kernel's consumer
-// warps); otherwise __syncthreads.  Warp partials go through `slot` / `xslot` (>= 32 entries no
-// concurrent reduction uses); every warp combines them with the same butterfly, so all threads
-// get identical bits and take the rare exact path together.
+// Sum over the `nt` threads of a row group (a multiple of 32; its warps are wbase, wbase + 1, ...
+// of the CTA, synchronised by group_sync(bar, nt)) of the squares of their vectors `v`, of which
+// each thread has formed the compensated partial sum `acc`; rounded as the exact sum would be.
+// Warp partials go through `slot` / `xslot` (indexed by the CTA's warp index; no concurrent
+// reduction of another group uses those entries); every warp combines them with the same
+// butterfly, so all threads get identical bits and take the rare exact path together.
 template <int VPT>
 __device__ __forceinline__ float block_sum_sq(const Sum2x2 &acc, const uint4 (&v)[VPT],
-                                              Sum2 *slot, ExactSlot *xslot, int nt, bool named)
+                                              Sum2 *slot, ExactSlot *xslot, int nt, int wbase,
+                                              int bar)
 {
     const Sum2 a = warp_sum(lanes_merged(acc));
     const int lane = threadIdx.x & 31;
     const int nw = nt >> 5;
     if (lane == 0)
         slot[threadIdx.x >> 5] = a;
-    if (named)
-        named_sync(1, nt);
-    else
-        __syncthreads();
-    Sum2 p = lane < nw ? slot[lane] : Sum2{0.0f, 0.0f};
+    group_sync(bar, nt);
+    Sum2 p = lane < nw ? slot[wbase + lane] : Sum2{0.0f, 0.0f};
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         if (off < nw) {
@@ -197,7 +200,7 @@ __device__ __forceinline__ float block_sum_sq(const Sum2x2 &acc, const uint4 (&v
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
         vv.v[i] = v[i];
-    return block_sum_exact<VPT>(vv, xslot, nt, named);
+    return block_sum_exact<VPT>(vv, xslot, nt, wbase, bar);
 }
 
 // Block-wide sum over `nt` threads of the squares of their vectors, in plain FP32 and a fixed
@@ -207,7 +210,7 @@ __device__ __forceinline__ float block_sum_sq(const Sum2x2 &acc, const uint4 (&v
 // BF16 ulp, unlike r, whose effect reaches h' through a sum that can cancel.
 template <int VPT>
 __device__ __forceinline__ float block_sum_sq_plain(const uint4 (&v)[VPT], float *slot, int nt,
-                                                    bool named)
+                                                    int wbase, int bar)
 {
     f2 s0 = 0ull, s1 = 0ull;
 #pragma unroll
@@ -228,13 +231,10 @@ __device__ __forceinline__ float block_sum_sq_plain(const uint4 (&v)[VPT], float
     const int nw = nt >> 5;
     if ((threadIdx.x & 31) == 0)
         slot[threadIdx.x >> 5] = t;
-    if (named)
-        named_sync(1, nt);
-    else
-        __syncthreads();
-    t = slot[0];
+    group_sync(bar, nt);
+    t = slot[wbase];
     for (int w = 1; w < nw; ++w)
-        t = __fadd_rn(t, slot[w]);
+        t = __fadd_rn(t, slot[wbase + w]);
     return t;
 }
 
@@ -254,30 +254,42 @@ __device__ __forceinline__ uint4 residual_operand_ieee(uint4 xh, float s)
 // Where a row's sublayer output comes from.
 constexpr int kSrcPlain = 0;  // x_in [T, H]
 constexpr int kSrcMoe = 1;    // the top-K combine of expert_out [T, K, H]
-constexpr int kSrcTp = 2;     // the rank-order sum of the P partials parts[p] [T, H]
+constexpr int kSrcTp = 2;     // the rank-order sum of the P partials TpParts::p[p] [T, H]
 
-// The boundary chain for one row whose inputs sit in registers: xv (x) and hv (h) hold this
-// thread's vectors tid + i * nt.  wpo(i) / wpr(i) give the matching weight vectors.
+// The extra kernel parameter of a row source: the partials for kSrcTp, nothing otherwise.
+struct NoParts {
+};
+template <int SRC>
+using SrcParts = typename std::conditional<SRC == kSrcTp, TpParts, NoParts>::type;
+
+__device__ __forceinline__ const void *part_ptr(const TpParts &x, int p) { return x.p[p]; }
+__device__ __forceinline__ const void *part_ptr(const NoParts &, int) { return nullptr; }
+
+// The boundary chain for one row whose inputs sit in registers: xv (x) and hv (h) hold the
+// vectors gtid + i * nt of thread gtid of the row's group (nt threads, warps wbase.. of the CTA,
+// barrier `bar`: see block_sum_sq).  wpo(i) / wpr(i) give the matching weight vectors.
 // `after_first_sum` runs right after the first block reduction.  `fail` (persistent kernels;
-// null otherwise) is the CTA's flag that a wait on its own copies ran out.  It is read after the
-// second block reduction, whose barrier follows every thread's waits for this row, and then
-// withholds this row's stores and those of every later row: no output is computed from a buffer
-// that may not have filled.
+// null otherwise) is the CTA's flag that a wait on its own copies ran out.  It is read right after
+// the first block reduction, whose barrier follows every thread's waits for this row (a thread
+// whose wait runs out raises the flag before it reaches that barrier), and then withholds this
+// row's stores and those of every later row: no output is computed from a buffer that may not
+// have filled.  Read there, the load overlaps the arithmetic of the rest of the chain.
 template <int VPT, typename WPost, typename WPre, typename AfterFirstSum>
 __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t row,
                                                const uint4 (&xv)[VPT], const uint4 (&hv)[VPT],
                                                WPost wpo, WPre wpr, Sum2 *red,
-                                               ExactSlot *xred, float *pred, int nt, bool named,
-                                               const volatile int *fail,
+                                               ExactSlot *xred, float *pred, int nt, int gtid,
+                                               int wbase, int bar, const volatile int *fail,
                                                AfterFirstSum after_first_sum)
 {
     const int nvec = a.H >> 3;
-    const int tid = threadIdx.x;
+    const int tid = gtid;
     const int64_t row_off = row * (int64_t)a.H;
 
     // ---- a1: r = 1/sqrt(mean(x^2) + eps) ---------------------------------------------------
-    const float r =
-        rms_inv(block_sum_sq(squares_sum(xv), xv, red, xred, nt, named), (float)a.H, a.eps);
+    const float r = rms_inv(block_sum_sq(squares_sum(xv), xv, red, xred, nt, wbase, bar),
+                            (float)a.H, a.eps);
+    const bool dead = fail != nullptr && *fail != 0;
     after_first_sum();
 
     // ---- a1 / a2: xhat = bf16((x r) w_post); h' = bf16(bf16(alpha h) + bf16(xhat / s)) -----
@@ -312,8 +324,9 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
             }
         }
     }
-    const f2 rr2 = splat(rms_inv(block_sum_sq_plain(hp, pred, nt, named), (float)a.H, a.eps));
-    if (fail != nullptr && *fail != 0)
+    const f2 rr2 =
+        splat(rms_inv(block_sum_sq_plain(hp, pred, nt, wbase, bar), (float)a.H, a.eps));
+    if (dead)
         return;  // a wait on this CTA's copies gave up: write nothing
 
     // ---- a3: y = bf16((h' r') w_pre); store h' and y -----------------------------------------
@@ -433,7 +446,7 @@ __device__ __forceinline__ void routing_coeffs(const BoundaryArgs &a, int64_t ro
 
 template <int VPT, int SRC>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
-    boundary_rows_kernel(const BoundaryArgs a)
+    boundary_rows_kernel(const BoundaryArgs a, const __grid_constant__ SrcParts<SRC> parts)
 {
     __shared__ Sum2 red[32];
     __shared__ ExactSlot xred[32];
@@ -468,7 +481,8 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
                                                2 * (size_t)a.H);
                 else if constexpr (SRC == kSrcTp)
                     xv[i] = reduce_vec<false>(a.P, [&](int p) {
-                        return (const unsigned char *)a.parts[p] + 2 * row_off + 16 * (int64_t)v;
+                        return (const unsigned char *)part_ptr(parts, p) + 2 * row_off +
+                               16 * (int64_t)v;
                     });
                 else
                     xv[i] = ld_stream((const char *)a.x_in + 2 * row_off + 16 * (int64_t)v);
@@ -479,7 +493,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
         }
         boundary_chain<VPT>(
             a, row, xv, hv, [&](int i) { return wpo[i]; }, [&](int i) { return wpr[i]; }, red,
-            xred, pred, nt, false, nullptr, [] {});
+            xred, pred, nt, tid, 0, 0, nullptr, [] {});
     }
 }
 
@@ -507,7 +521,8 @@ constexpr int kRingCtasPerSm = 3;
 
 template <int NC, int VPT, int MINB, int SRC>
 __global__ void __launch_bounds__(NC + 32, MINB)
-    ring_kernel(const BoundaryArgs a, int stages, bool starve)
+    ring_kernel(const BoundaryArgs a, const __grid_constant__ SrcParts<SRC> parts, int stages,
+                bool starve)
 {
     extern __shared__ __align__(128) unsigned char dyn[];
     uint64_t *full = reinterpret_cast<uint64_t *>(dyn);
@@ -556,7 +571,10 @@ __global__ void __launch_bounds__(NC + 32, MINB)
         for (int64_t u = 0; u < my_units; ++u) {
             if (*vfail)
                 break;  // a consumer gave up waiting: issue nothing more
-            // the stage's previous use (pass - 1) must have been released by the consumers
+            // the stage's previous use (pass - 1) must have been released by the consumers.  A
+            // consumer warp releases a stage only after its wait on it succeeded, so a released
+            // stage's `full` phase is complete and re-arming it is legal; after a failed wait
+            // the release never comes and this wait returns false once `fail` is up.
             if (pass > 0 && !mbar_wait_or_fail(&empty[st], (pass - 1) & 1u, &fail, a.wait_ns))
                 break;
             const int nv = nvec - c * NC < NC ? nvec - c * NC : NC;
@@ -565,11 +583,15 @@ __global__ void __launch_bounds__(NC + 32, MINB)
             const size_t col = (size_t)c * kSlice;
             mbar_arrive_expect_tx(&full[st], (uint32_t)(KIN + 1) * bytes);
             if (!starve) {
-                for (int k = 0; k < KIN; ++k) {
-                    const char *src =
-                        SRC == kSrcTp ? (const char *)a.parts[k] + (size_t)row * 2 * a.H
-                                      : (const char *)a.expert_out + ((size_t)row * KIN + k) * 2 * a.H;
-                    bulk_g2s(dst + (size_t)k * kSlice, src + col, bytes, &full[st]);
+#pragma unroll
+                for (int k = 0; k < kRingMaxK; ++k) {  // static slot indices: no local copies
+                    if (k < KIN) {
+                        const char *src =
+                            SRC == kSrcTp
+                                ? (const char *)part_ptr(parts, k) + (size_t)row * 2 * a.H
+                                : (const char *)a.expert_out + ((size_t)row * KIN + k) * 2 * a.H;
+                        bulk_g2s(dst + (size_t)k * kSlice, src + col, bytes, &full[st]);
+                    }
                 }
                 bulk_g2s(dst + (size_t)KIN * kSlice,
                          (const char *)a.h_in + (size_t)row * 2 * a.H + col, bytes, &full[st]);
@@ -623,7 +645,7 @@ __global__ void __launch_bounds__(NC + 32, MINB)
         uint4 xv[VPT], hv[VPT];
 #pragma unroll
         for (int ch = 0; ch < VPT; ++ch) {
-            (void)mbar_wait_or_fail(&full[st], parity, &fail, a.wait_ns);
+            const bool landed = mbar_wait_or_fail(&full[st], parity, &fail, a.wait_ns);
             const unsigned char *stage = ring + (size_t)st * stage_bytes;
             if (ch * NC + tid < nvec) {
                 hv[ch] = *reinterpret_cast<const uint4 *>(stage + (size_t)KIN * kSlice + 16 * tid);
@@ -637,7 +659,7 @@ __global__ void __launch_bounds__(NC + 32, MINB)
                 hv[ch] = xv[ch];
             }
             __syncwarp();
-            if (lane == 0)
+            if (lane == 0 && landed)
                 mbar_arrive(&empty[st]);  // this warp is done with the stage
             if (++st == stages) {
                 st = 0;
@@ -646,8 +668,8 @@ __global__ void __launch_bounds__(NC + 32, MINB)
         }
         boundary_chain<VPT>(
             a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
-            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, true, vfail,
-            [] {});
+            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, tid, 0, 1,
+            vfail, [] {});
     }
     if (tid == 0 && *vfail)
         atomicOr(&g_fault_word, kFaultCopyTimeout);
@@ -660,16 +682,17 @@ __global__ void __launch_bounds__(NC + 32, MINB)
 // "full" mbarrier per buffer.  Thread t owns vectors t + c * NC of a row.  Right after the first
 // block reduction of a row -- when every thread has read the row out of its buffer, since the
 // reduction's barrier follows the reads -- thread 0 refills that buffer with the row NBUF rows
-// ahead, so the copies fly during the rest of the row's chain and the next rows'.  With the norm
-// weights parked in shared memory too (WSMEM), a row buffer and the weights take 40 KB for
-// H = 5120, and 4 CTAs of 4 warps fit on an SM at up to 128 registers a thread.
+// ahead, so the copies fly during the rest of the row's chain and the next rows'.  The norm
+// weights are parked in shared memory too: a row buffer and the weights take 40 KB for H = 5120.
 //
 // Once a wait has run out (the CTA's `fail` flag), thread 0 refills nothing more, so at most one
-// copy per buffer can still be in flight, and the row loop writes nothing.  `starve` (the
+// copy per buffer can still be in flight, and the row loop writes nothing.  A refill re-arms its
+// buffer's barrier only after thread 0's own wait on that buffer succeeded (the phase is
+// complete): otherwise the flag is up by then, read after the reduction's barrier.  `starve` (the
 // diagnostic beam_selftest_persistent_timeout) arms the buffers' barriers without issuing the
 // copies.
 
-template <int VPT, int NBUF, bool WSMEM>
+template <int VPT, int NBUF>
 __global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs a, bool starve)
 {
     constexpr int NC = 128;
@@ -706,12 +729,10 @@ __global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs 
         fail = 0;
         fence_mbar_init();
     }
-    if constexpr (WSMEM) {
 #pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-            wsm[i * NC + tid] = weight_vec(a.w_post, tid + i * NC, nvec);
-            wsm[(VPT + i) * NC + tid] = weight_vec(a.w_pre, tid + i * NC, nvec);
-        }
+    for (int i = 0; i < VPT; ++i) {
+        wsm[i * NC + tid] = weight_vec(a.w_post, tid + i * NC, nvec);
+        wsm[(VPT + i) * NC + tid] = weight_vec(a.w_pre, tid + i * NC, nvec);
     }
     __syncthreads();
     pdl_wait();
@@ -741,14 +762,9 @@ __global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs 
         }
         const bool refill = i + NBUF < my_rows;
         boundary_chain<VPT>(
-            a, row, xv, hv,
-            [&](int k) {
-                return WSMEM ? wsm[k * NC + tid] : weight_vec(a.w_post, tid + k * NC, nvec);
-            },
-            [&](int k) {
-                return WSMEM ? wsm[(VPT + k) * NC + tid] : weight_vec(a.w_pre, tid + k * NC, nvec);
-            },
-            red, xred, pred, NC, false, vfail, [&] {
+            a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
+            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, tid, 0, 0,
+            vfail, [&] {
                 if (tid == 0 && refill && !*vfail) {
                     issue(row + NBUF * stride, b);
                     ++refills;
@@ -821,8 +837,8 @@ cudaError_t persistent_blocks(const void *kern, int threads, size_t smem, int *p
 }
 
 template <int NC, int VPT, int MINB, int SRC>
-cudaError_t launch_ring(const BoundaryArgs &a, int stages, size_t smem, int sms, bool starve,
-                        cudaStream_t stream)
+cudaError_t launch_ring(const BoundaryArgs &a, const SrcParts<SRC> &parts, int stages,
+                        size_t smem, int sms, bool starve, cudaStream_t stream)
 {
     auto kern = ring_kernel<NC, VPT, MINB, SRC>;
     const int threads = NC + 32;
@@ -834,7 +850,7 @@ cudaError_t launch_ring(const BoundaryArgs &a, int stages, size_t smem, int sms,
         return cudaErrorInvalidConfiguration;
     const int64_t slots = (int64_t)sms * per_sm;
     const unsigned grid = (unsigned)(a.T < slots ? a.T : slots);
-    e = launch_pdl(kern, dim3(grid), dim3(threads), smem, stream, a, stages, starve);
+    e = launch_pdl(kern, dim3(grid), dim3(threads), smem, stream, a, parts, stages, starve);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -859,8 +875,8 @@ inline int round_warps(int n) { return (n + 31) / 32 * 32; }
 // only because the kernel's static arrays are sized for its 4 consumer warps (with a third stage
 // the ring no longer runs dry while the consumers finish a row's chain: 0.93 -> 0.98).
 template <int NC, int MINB, int SRC>
-cudaError_t launch_ring_chunks(const BoundaryArgs &a, int chunks, int sms, bool starve,
-                               cudaStream_t stream)
+cudaError_t launch_ring_chunks(const BoundaryArgs &a, const SrcParts<SRC> &parts, int chunks,
+                               int sms, bool starve, cudaStream_t stream)
 {
     const int stages = 3;
     const int kin = SRC == kSrcTp ? a.P : a.K;
@@ -868,30 +884,29 @@ cudaError_t launch_ring_chunks(const BoundaryArgs &a, int chunks, int sms, bool 
     const size_t weights = (size_t)2 * chunks * NC * 16;
     const size_t smem = kRingHeader + stages * stage + weights;
     switch (chunks) {
-    case 1: return launch_ring<NC, 1, MINB, SRC>(a, stages, smem, sms, starve, stream);
-    case 2: return launch_ring<NC, 2, MINB, SRC>(a, stages, smem, sms, starve, stream);
-    case 3: return launch_ring<NC, 3, MINB, SRC>(a, stages, smem, sms, starve, stream);
-    case 4: return launch_ring<NC, 4, MINB, SRC>(a, stages, smem, sms, starve, stream);
-    case 5: return launch_ring<NC, 5, MINB, SRC>(a, stages, smem, sms, starve, stream);
-    case 6: return launch_ring<NC, 6, MINB, SRC>(a, stages, smem, sms, starve, stream);
-    case 7: return launch_ring<NC, 7, MINB, SRC>(a, stages, smem, sms, starve, stream);
-    default: return launch_ring<NC, 8, MINB, SRC>(a, stages, smem, sms, starve, stream);
+    case 1: return launch_ring<NC, 1, MINB, SRC>(a, parts, stages, smem, sms, starve, stream);
+    case 2: return launch_ring<NC, 2, MINB, SRC>(a, parts, stages, smem, sms, starve, stream);
+    case 3: return launch_ring<NC, 3, MINB, SRC>(a, parts, stages, smem, sms, starve, stream);
+    case 4: return launch_ring<NC, 4, MINB, SRC>(a, parts, stages, smem, sms, starve, stream);
+    case 5: return launch_ring<NC, 5, MINB, SRC>(a, parts, stages, smem, sms, starve, stream);
+    case 6: return launch_ring<NC, 6, MINB, SRC>(a, parts, stages, smem, sms, starve, stream);
+    case 7: return launch_ring<NC, 7, MINB, SRC>(a, parts, stages, smem, sms, starve, stream);
+    default: return launch_ring<NC, 8, MINB, SRC>(a, parts, stages, smem, sms, starve, stream);
     }
 }
 
-// Row buffers and whether the weights are parked in shared memory, for the prefetch kernel: two
-// buffers and the weights (60 KB for H = 5120, 3 CTAs per SM) were the fastest of the shapes
-// measured; without the weights in shared memory the long-latency weight loads inside the chain
-// cost 15%.
+// Row buffers of the prefetch kernel, with the weights parked in shared memory: two buffers
+// and the weights (60 KB for H = 5120, 3 CTAs per SM) were the fastest of the shapes measured;
+// without the weights in shared memory the long-latency weight loads inside the chain cost 15%,
+// and two 4-warp row groups per CTA sharing one copy of the weights (four rows in flight per SM
+// instead of three) took 117.7 us against 108.8 us at T = 16384.
 constexpr int kPfBuffers = 2;
-constexpr bool kPfWeightsInSmem = true;
 
 template <int VPT>
 cudaError_t launch_pf_vpt(const BoundaryArgs &a, int sms, bool starve, cudaStream_t stream)
 {
-    auto kern = boundary_pf_kernel<VPT, kPfBuffers, kPfWeightsInSmem>;
-    const size_t smem = (size_t)kPfBuffers * 2 * VPT * 128 * 16 +
-                        (kPfWeightsInSmem ? (size_t)2 * VPT * 128 * 16 : 0);
+    auto kern = boundary_pf_kernel<VPT, kPfBuffers>;
+    const size_t smem = (size_t)kPfBuffers * 2 * VPT * 128 * 16 + (size_t)2 * VPT * 128 * 16;
     int per_sm = 0;
     cudaError_t e = persistent_blocks((const void *)kern, 128, smem, &per_sm);
     if (e != cudaSuccess)
@@ -920,7 +935,7 @@ cudaError_t launch_pf(const BoundaryArgs &a, int chunks, int sms, bool starve,
 }
 
 template <int SRC>
-cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
+cudaError_t launch(const BoundaryArgs &a, const SrcParts<SRC> &parts, cudaStream_t stream)
 {
     const int nvec = a.H / 8;
     const int sms = device_sms();
@@ -933,8 +948,8 @@ cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
         if constexpr (SRC == kSrcPlain)
             return launch_pf(a, chunks, sms, false, stream);
         else
-            return launch_ring_chunks<kRingConsumers, kRingCtasPerSm, SRC>(a, chunks, sms, false,
-                                                                            stream);
+            return launch_ring_chunks<kRingConsumers, kRingCtasPerSm, SRC>(a, parts, chunks, sms,
+                                                                            false, stream);
     }
     // Few rows (or very wide rows, or more than 8 slots): one CTA per row straight from memory.
     // Blocks of at most 512 threads for few rows (320 for H = 5120, two vectors a thread: a
@@ -947,10 +962,22 @@ cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
     const dim3 grid((unsigned)(a.T < (int64_t)(1 << 30) ? a.T : (int64_t)(1 << 30)));
     cudaError_t e;
     switch (vpt) {
-    case 1: e = launch_pdl(boundary_rows_kernel<1, SRC>, grid, dim3(threads), 0, stream, a); break;
-    case 2: e = launch_pdl(boundary_rows_kernel<2, SRC>, grid, dim3(threads), 0, stream, a); break;
-    case 4: e = launch_pdl(boundary_rows_kernel<4, SRC>, grid, dim3(threads), 0, stream, a); break;
-    default: e = launch_pdl(boundary_rows_kernel<8, SRC>, grid, dim3(threads), 0, stream, a); break;
+    case 1:
+        e = launch_pdl(boundary_rows_kernel<1, SRC>, grid, dim3(threads), 0, stream, a,
+                       parts);
+        break;
+    case 2:
+        e = launch_pdl(boundary_rows_kernel<2, SRC>, grid, dim3(threads), 0, stream, a,
+                       parts);
+        break;
+    case 4:
+        e = launch_pdl(boundary_rows_kernel<4, SRC>, grid, dim3(threads), 0, stream, a,
+                       parts);
+        break;
+    default:
+        e = launch_pdl(boundary_rows_kernel<8, SRC>, grid, dim3(threads), 0, stream, a,
+                       parts);
+        break;
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -959,17 +986,18 @@ cudaError_t launch(const BoundaryArgs &a, cudaStream_t stream)
 
 cudaError_t launch_boundary(const BoundaryArgs &a, cudaStream_t stream)
 {
-    return launch<kSrcPlain>(a, stream);
+    return launch<kSrcPlain>(a, NoParts{}, stream);
 }
 
 cudaError_t launch_moe_boundary(const BoundaryArgs &a, cudaStream_t stream)
 {
-    return launch<kSrcMoe>(a, stream);
+    return launch<kSrcMoe>(a, NoParts{}, stream);
 }
 
-cudaError_t launch_allreduce_boundary(const BoundaryArgs &a, cudaStream_t stream)
+cudaError_t launch_allreduce_boundary(const BoundaryArgs &a, const TpParts &parts,
+                                      cudaStream_t stream)
 {
-    return launch<kSrcTp>(a, stream);
+    return launch<kSrcTp>(a, parts, stream);
 }
 
 cudaError_t launch_persistent_starved(const BoundaryArgs &a, bool moe, cudaStream_t stream)
@@ -977,8 +1005,8 @@ cudaError_t launch_persistent_starved(const BoundaryArgs &a, bool moe, cudaStrea
     const int chunks = (a.H / 8 + 127) / 128;
     const int sms = device_sms();
     if (moe)
-        return launch_ring_chunks<kRingConsumers, kRingCtasPerSm, kSrcMoe>(a, chunks, sms, true,
-                                                                            stream);
+        return launch_ring_chunks<kRingConsumers, kRingCtasPerSm, kSrcMoe>(a, NoParts{}, chunks,
+                                                                            sms, true, stream);
     return launch_pf(a, chunks, sms, true, stream);
 }
 

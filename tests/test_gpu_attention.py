@@ -58,11 +58,13 @@ def test_head_counts(kind, nq, nk):
 
 @pytest.mark.parametrize("kind", ["rope", "ssmax"])
 @pytest.mark.parametrize("T,nq,nk", [(609, 48, 8), (1999, 48, 8), (1001, 3, 2), (1001, 1, 0),
-                                     (1001, 0, 1), (1001, 64, 8)])
+                                     (1001, 0, 1), (1001, 64, 8), (4901, 48, 8), (4901, 3, 2),
+                                     (4901, 1, 0), (4901, 64, 8)])
 def test_many_tokens_ragged_tails(kind, T, nq, nk):
-    # From 4 x 152 tokens on, the multi-token tiles (8 tokens for RoPE, whose kernel stages the
-    # next pass in shared memory; 4 for SSMax), with ragged last tiles and passes, and head counts
-    # whose items do not fill a pass.
+    # SSMax takes 4-token tiles from 4 tokens per SM on; RoPE one-token tiles up to 32 tokens per
+    # SM and from there (4901 on a 152-SM GB300) the staged kernel's 8-token tiles, which copy the
+    # next pass into shared memory: ragged last tiles and passes, and head counts whose items do
+    # not fill a pass.
     c = bi.attn_qk_case(T=T, n_q=nq, n_kv=nk, seed=T + nq + nk)
     q = dev(c["q"]) if nq else torch.empty((T, 0, D), dtype=torch.bfloat16, device="cuda")
     k = dev(c["k"]) if nk else torch.empty((T, 0, D), dtype=torch.bfloat16, device="cuda")
@@ -74,7 +76,7 @@ def test_many_tokens_ragged_tails(kind, T, nq, nk):
 
 
 @pytest.mark.parametrize("kind", ["rope", "ssmax"])
-@pytest.mark.parametrize("T", [37, 1001])
+@pytest.mark.parametrize("T", [37, 1001, 4901])
 def test_views_into_packed_qkv_gate_projection(kind, T):
     # One packed [T, (48 + 8 + 8) * 128 + 48 * 128] projection output (Q | K | V | gate):
     # Q and K are row-strided views; V and the gate columns must stay untouched.
@@ -106,7 +108,7 @@ def test_rope_theta_and_special_positions():
 
 
 @pytest.mark.parametrize("kind", ["rope", "ssmax"])
-@pytest.mark.parametrize("T", [5, 1001])
+@pytest.mark.parametrize("T", [5, 1001, 4901])
 def test_extreme_and_nonfinite_heads(kind, T):
     # Heads whose sum of squares sits near the top of the FP32 range, overflows, is NaN, is zero
     # or underflows; every other head random.  The kernels must give the oracle's IEEE results.
@@ -136,7 +138,7 @@ def test_extreme_and_nonfinite_heads(kind, T):
 
 
 @pytest.mark.parametrize("kind", ["rope", "ssmax"])
-@pytest.mark.parametrize("T", [5, 1001])
+@pytest.mark.parametrize("T", [5, 1001, 4901])
 @pytest.mark.parametrize("eps", [0.0, 1e-2])
 def test_eps_zero_and_large(kind, T, eps):
     # eps = 0: an all-zero head has r = 1/sqrt(0) = inf and NaN outputs, as in the oracle;
@@ -312,38 +314,43 @@ def _tie_heads(T, nh, seed, nudge_every=2):
     taken from another quad, or one that misses a lane, moves r by far more than a BF16 ulp."""
     from fractions import Fraction
     g = np.random.Generator(np.random.PCG64(seed))
-    x = np.zeros((T, nh, D), np.float32)
-    for t in range(T):
-        for h in range(nh):
-            m, e = (t * 7 + h * 3) % 8, (t + h) % 6 - 3
-            a = np.float32((1 + m / 8) * 2.0 ** e)
-            s0 = Fraction(4) * Fraction(float(a)) ** 2
-            E = int(np.floor(np.log2(float(s0))))
-            if E % 2 == 0:
-                nb, b = 16, np.float32(2.0 ** ((E - 28) // 2))    # 16 b^2 = 2^(E-24)
-            else:
-                nb, b = 8, np.float32(2.0 ** ((E - 27) // 2))     # 8 b^2 = 2^(E-24)
-            off = h % 8
-            sign = lambda: np.float32(1.0 if g.random() < 0.5 else -1.0)  # noqa: E731
-            for v in range(4):
-                x[t, h, 8 * v + off] = sign() * a
-            for i in range(nb):
-                x[t, h, 8 * i + (off + 1) % 8] = sign() * b
-            nudged = (t * nh + h) % nudge_every == 0
-            if nudged:
-                x[t, h, 120 + (off + 2) % 8] = np.float32(2.0 ** (E // 2 - 30))
-            if (t * nh + h) % 13 == 0:
-                # the construction: S = S0 + ulp(S0)/2 (+ t^2), an FP32 midpoint (or just above)
-                ssum = sum(Fraction(float(v)) ** 2 for v in x[t, h])
-                half = Fraction(2) ** (E - 24)
-                assert ssum - s0 == half + (Fraction(float(2.0 ** (E // 2 - 30))) ** 2
-                                            if nudged else 0)
-    return oracle.bf16_rne(x)
+    x = np.zeros((T, nh, D), np.float64)
+    t_i, h_i = np.meshgrid(np.arange(T), np.arange(nh), indexing="ij")
+    m, e = (t_i * 7 + h_i * 3) % 8, (t_i + h_i) % 6 - 3
+    a = (1 + m / 8) * 2.0 ** e                       # 4 significant bits: a^2 exact
+    E = np.floor(np.log2(4 * a * a)).astype(np.int64)  # 4 a^2 in [2^E, 2^(E+1))
+    even = E % 2 == 0
+    b = np.where(even, 2.0 ** ((E - 28) // 2), 2.0 ** ((E - 27) // 2))  # 16 or 8 b^2 = 2^(E-24)
+    nb = np.where(even, 16, 8)
+    off = h_i % 8
+    sign = lambda shape: np.where(g.random(shape) < 0.5, -1.0, 1.0)  # noqa: E731
+    tt, hh = t_i.ravel(), h_i.ravel()
+    for v in range(4):
+        x[tt, hh, 8 * v + off.ravel()] = (a * sign(a.shape)).ravel()
+    for i in range(16):
+        sel = (nb > i).ravel()
+        x[tt[sel], hh[sel], (8 * i + (off + 1) % 8).ravel()[sel]] = (b * sign(b.shape)).ravel()[sel]
+    nudged = ((t_i * nh + h_i) % nudge_every == 0)
+    tiny = 2.0 ** (E // 2 - 30)
+    sel = nudged.ravel()
+    x[tt[sel], hh[sel], (120 + (off + 2) % 8).ravel()[sel]] = tiny.ravel()[sel]
+    # the construction, checked in exact rationals on a sample of heads: S = S0 + ulp(S0)/2
+    # (+ t^2), an FP32 midpoint (or just above)
+    for k in range(0, T * nh, max(1, T * nh // 200)):
+        t, h = divmod(k, nh)
+        ssum = sum(Fraction(float(v)) ** 2 for v in x[t, h] if v != 0)
+        s0 = 4 * Fraction(float(a[t, h])) ** 2
+        want = s0 + Fraction(2) ** int(E[t, h] - 24)
+        if nudged[t, h]:
+            want += Fraction(float(tiny[t, h])) ** 2
+        assert ssum == want
+    return oracle.bf16_rne(x.astype(np.float32))
 
 
 @pytest.mark.parametrize("T,nq,nk", [(5, 48, 8), (5, 3, 2), (4, 5, 0), (3, 1, 1),
                                      (4 * 152 + 3, 48, 8), (4 * 152 + 3, 3, 2),
-                                     (4 * 152 + 5, 1, 1)])
+                                     (4 * 152 + 5, 1, 1), (32 * 152 + 3, 48, 8),
+                                     (32 * 152 + 5, 3, 2)])
 def test_near_tie_heads_in_every_quad_position(T, nq, nk):
     # RoPE head sums at an FP32 rounding midpoint, in every quad position of every warp, beside
     # inactive quads (head counts that leave a pass ragged: 3 + 2, 5 + 0, 1 + 1 heads, and a last

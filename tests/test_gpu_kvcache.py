@@ -87,7 +87,8 @@ def check_caches(kind, c, kv, fp8, got, k_scale=1.0, v_scale=1.0, what=""):
 
 @pytest.mark.parametrize("kind", ["rope", "ssmax"])
 @pytest.mark.parametrize("fp8", [False, True])
-@pytest.mark.parametrize("T,mode", [(128, "uniform"), (2048, "contiguous"), (1999, "uniform")])
+@pytest.mark.parametrize("T,mode", [(128, "uniform"), (2048, "contiguous"), (1999, "uniform"),
+                                    (4901, "uniform")])
 def test_qk_kv_configs(kind, fp8, T, mode):
     lib()
     c = bi.attn_qk_case(T=T, seed=T + 1, pos_mode=mode)
@@ -97,7 +98,7 @@ def test_qk_kv_configs(kind, fp8, T, mode):
 
 @pytest.mark.parametrize("kind", ["rope", "ssmax"])
 @pytest.mark.parametrize("k_scale,v_scale", [(0.5, 4.0), (3.0, 0.3)])
-@pytest.mark.parametrize("T", [64, 1001])
+@pytest.mark.parametrize("T", [64, 1001, 4901])
 def test_fp8_scales_power_of_two_and_general(kind, k_scale, v_scale, T):
     # T = 1001: the staged kernel, with a ragged last tile
     c = bi.attn_qk_case(T=T, seed=5)
@@ -107,7 +108,7 @@ def test_fp8_scales_power_of_two_and_general(kind, k_scale, v_scale, T):
                  what=f"scales {k_scale},{v_scale} T={T}")
 
 
-@pytest.mark.parametrize("T", [9, 1001])
+@pytest.mark.parametrize("T", [9, 1001, 4901])
 @pytest.mark.parametrize("nq,nk", [(1, 1), (3, 2), (64, 8), (0, 3), (5, 0)])
 def test_head_counts_with_cache(nq, nk, T):
     c = bi.attn_qk_case(T=T, n_q=nq, n_kv=nk, seed=nq * 7 + nk)
@@ -120,7 +121,7 @@ def test_head_counts_with_cache(nq, nk, T):
         check_caches("rope", c, kv, fp8, got, what=f"{nq}/{nk} fp8={fp8}")
 
 
-@pytest.mark.parametrize("T", [33, 1001])
+@pytest.mark.parametrize("T", [33, 1001, 4901])
 def test_views_into_packed_qkv_projection(T):
     # Q, K and V as row-strided views of one packed [T, (48 + 8 + 8) * 128] projection output
     c = bi.attn_qk_case(T=T, seed=8)
