@@ -880,17 +880,15 @@ def run_gpu_arm(args) -> None:
     step = Step(host, device)
     torch.cuda.synchronize(device)
 
-    for i in range(args.warmup):
-        step.launch(i)
-    torch.cuda.synchronize(device)
-
     nk = len(KERNELS)
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.3)  # let the sampler come up before the timed region
-    # The timed region: K steps, with events only at its two ends.  An event recorded between two
-    # launches breaks their programmatic dependency (the second launch then waits for the first
-    # to finish instead of starting early), so per-kernel events would slow the step they time.
+    time.sleep(0.3)  # let the sampler come up before the warm-up steps (the GPU idles meanwhile)
+    for i in range(args.warmup):
+        step.launch(i)
+    torch.cuda.synchronize(device)
+    # The timed region: K steps, with events only at its two ends (nothing between the launches of
+    # the step but the launches themselves).
     t0_ev, t1_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize(device)
@@ -909,8 +907,7 @@ def run_gpu_arm(args) -> None:
     T = step.T
     value = whole_job_rate(ws, T, args.steps, max_ms)
 
-    # The same K steps again with an event between kernels: each kernel's time inside the step
-    # (without the overlap of its start with its predecessor's end that the events remove).
+    # The same K steps again with an event between kernels: each kernel's time inside the step.
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
     torch.cuda.synchronize(device)
     for i in range(args.steps):
@@ -933,9 +930,8 @@ def run_gpu_arm(args) -> None:
                 "algorithmic_bytes_per_launch": in_step[dom]["bytes_per_launch"],
                 "launches_timed": args.steps,
                 "how": "algorithmic bytes / mean launch time of the kernel over the K steps run "
-                       "again with a CUDA event between kernels (on the launching stream); the "
-                       "events cost each launch its overlap with the previous one, so this is a "
-                       "lower bound; 'isolated' is the kernel alone over back-to-back launches"}
+                       "again with a CUDA event between kernels (on the launching stream); "
+                       "'isolated' is the kernel alone over back-to-back launches"}
     tr = profiled_traffic(dom, T)
     if tr:
         roofline.update(tr)

@@ -94,6 +94,15 @@ __device__ __forceinline__ float head_sum_exact(const char *row, int q, unsigned
     return exact_round(acc, emax);
 }
 
+// Two FP32 pairs from four consecutive floats in shared memory (16-byte aligned): one 16-byte
+// load in place of two 8-byte ones.
+__device__ __forceinline__ void lds_f2x2(const float *p, f2 &a, f2 &b)
+{
+    const float4 v = *reinterpret_cast<const float4 *>(p);
+    a = make_f2(v.x, v.y);
+    b = make_f2(v.z, v.w);
+}
+
 // One 8-element vector of BF16 values `o` into a KV cache at element offset `e`: the BF16 bits
 // (mode 1), or FP8 E4M3 of value / scale (mode 2; round to nearest even, saturating).  The
 // quotient is IEEE division, or a product by the exact reciprocal where the scale is a power of
@@ -266,9 +275,11 @@ __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], ch
     for (int jj = 0; jj < 4; ++jj) {
         const int e0 = 8 * (q + 4 * jj);
 #pragma unroll
-        for (int pp = 0; pp < 4; ++pp) {
-            const f2 w = *reinterpret_cast<const f2 *>(&wrow[e0 + 2 * pp]);
-            qh[jj][pp] = mul2(mul2(x[jj][pp], rr), w);
+        for (int pp = 0; pp < 4; pp += 2) {
+            f2 w0, w1;
+            lds_f2x2(&wrow[e0 + 2 * pp], w0, w1);
+            qh[jj][pp] = mul2(mul2(x[jj][pp], rr), w0);
+            qh[jj][pp + 1] = mul2(mul2(x[jj][pp + 1], rr), w1);
         }
     }
     f2 out[4][4];
@@ -276,10 +287,14 @@ __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], ch
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
             const int i0 = 8 * (q + 4 * jj);  // first-half element index (< 64)
+            f2 cc[4], ss[4];
+            lds_f2x2(&cst[i0], cc[0], cc[1]);
+            lds_f2x2(&cst[i0 + 4], cc[2], cc[3]);
+            lds_f2x2(&snt[i0], ss[0], ss[1]);
+            lds_f2x2(&snt[i0 + 4], ss[2], ss[3]);
 #pragma unroll
             for (int pp = 0; pp < 4; ++pp) {
-                const f2 c = *reinterpret_cast<const f2 *>(&cst[i0 + 2 * pp]);
-                const f2 sv = *reinterpret_cast<const f2 *>(&snt[i0 + 2 * pp]);
+                const f2 c = cc[pp], sv = ss[pp];
                 const f2 lo = qh[jj][pp], hi = qh[jj + 2][pp];
                 // out_i = q_i c - q_{i+64} s;  out_{i+64} = q_{i+64} c + q_i s, each product
                 // rounded.  A packed product that feeds a packed add is fused into one FMA by the
@@ -468,35 +483,38 @@ __global__ void __launch_bounds__(kQkThreads, KV ? 3 : 4)
         const int nt = (int)(a.T - t0 < TT ? a.T - t0 : TT);
         const int nitems = nt * nheads;
         const int npass = (nitems + kSlots - 1) / kSlots;
-        // item of pass p for this quad: token tt and head hd of the tile, or none
+        // item of pass p for this quad: token tt and head hd of the tile, or none; located once,
+        // when its copies are issued, and carried to the pass that processes it
         auto locate = [&](int p, int &tt, int &hd) -> char * {
             const int j = p * kSlots + slot;
             item_of(j, nitems, nheads, hmag, tt, hd);
             return j < nitems ? item_row(a, t0 + tt, hd, nqk) : nullptr;
         };
-        auto issue = [&](int p) {
-            int tt, hd;
-            const char *row = locate(p, tt, hd);
+        auto issue = [&](int p, const char *row) {
             if (row)
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
                     cp_async16(&stage[p & 1][jj][tid], row + 16 * (q + 4 * jj));
             cp_async_commit();
         };
-        issue(0);
+        int tt_n, hd_n;
+        char *row_n = locate(0, tt_n, hd_n);
+        issue(0, row_n);
         for (int p = 0; p < npass; ++p) {
-            if (p + 1 < npass)
-                issue(p + 1);
-            else
+            const int tt = tt_n, hd = hd_n;
+            char *row = row_n;
+            if (p + 1 < npass) {
+                row_n = locate(p + 1, tt_n, hd_n);
+                issue(p + 1, row_n);
+            } else {
                 cp_async_commit();  // an empty group keeps "all but the newest" meaning pass p
+            }
             if (p == 0) {  // the tile's factors, while the first copies fly
                 tile_factors<ROPE, KV, TT>(a, tab, t0, nt, cs[buf], sn[buf], scale_q[buf],
                                            tslot[buf]);
                 __syncthreads();
             }
             cp_async_wait_one();
-            int tt, hd;
-            char *row = locate(p, tt, hd);
             uint4 v[4];
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj)
