@@ -142,3 +142,24 @@ def test_zero_tokens():
     w = torch.ones(5120, dtype=torch.bfloat16, device="cuda")
     rsn.beam_allreduce_boundary_fwd(h, h, h, [h, h], w, w, 3)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("which", ["rows", "persistent"])
+def test_nonfinite_overflowing_and_zero_partials(which):
+    # NaN in one rank, +inf and -inf in others (separately, and meeting in one element: NaN), the
+    # largest finite BF16 in every rank (the FP32 sum overflows to inf), all-zero and all -0
+    # rows; the rest random.  IEEE results, as the oracle's.
+    T = 8 if which == "rows" else persistent_T()
+    c = bi.allreduce_case(T=T, P=4, n=5, seed=21)
+    p = u16(c["parts"]).copy()
+    p[0, 0, 3] = 0x7FC0                    # NaN
+    p[1, 1, 7] = 0x7F80                    # +inf
+    p[2, 1, 9] = 0xFF80                    # -inf
+    p[1, 2, 11], p[3, 2, 11] = 0x7F80, 0xFF80   # +inf + -inf
+    p[:, 3, :] = 0x7F7F                    # 4 x the largest finite BF16: inf in FP32
+    p[:, 4, :] = 0                         # a zero row: r = 1/sqrt(eps)
+    p[:, 5, :] = 0x8000                    # -0 in every rank
+    p[:2, 6, :] = 0x5F34                   # two ranks of 1.3e19: squares near the FP32 top
+    p[2:, 6, :] = 0
+    c["parts"] = bi.from_u16(p)
+    check(run_gpu(c), oracle_run(c), f"non-finite partials ({which})")
