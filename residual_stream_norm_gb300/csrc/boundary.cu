@@ -511,6 +511,14 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
 // issuing the copies and reads no routing weights: the consumers' first wait runs out after
 // a.wait_ns, and the kernel writes nothing.
 
+// The persistent kernels (this ring and the prefetch kernel below) let the next kernel of their
+// stream be launched only once a CTA has finished its rows (griddepcontrol.launch_dependents at
+// the end), not at its start as the other kernels do: a persistent grid is resident all at once,
+// so an early signal let the next kernel's CTAs be placed beside it while it ran.  In the
+// five-kernel prefill step that cost 41 us of 669 (boundary -> MoE boundary pairs took 540 us
+// against 379, MoE boundary -> Q/K RoPE 516 against 357); each kernel alone loses about 1-2 us of
+// overlap with its own next launch instead.
+
 constexpr int kRingMaxStages = 4;
 constexpr int kRingHeader = 2 * kRingMaxStages * 8;  // the full and empty mbarriers
 
@@ -547,7 +555,6 @@ __global__ void __launch_bounds__(NC + 32, MINB)
     const int64_t my_rows = first < a.T ? (a.T - first + stride - 1) / stride : 0;
     const int64_t my_units = my_rows * VPT;
 
-    pdl_launch_dependents();
     if (tid == 0) {
         for (int st = 0; st < stages; ++st) {
             mbar_init(&full[st], 1);
@@ -671,6 +678,7 @@ __global__ void __launch_bounds__(NC + 32, MINB)
             [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, tid, 0, 1,
             vfail, [] {});
     }
+    pdl_launch_dependents();  // only now (see the note above the ring kernel)
     if (tid == 0 && *vfail)
         atomicOr(&g_fault_word, kFaultCopyTimeout);
 }
@@ -722,7 +730,6 @@ __global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs 
         }
     };
 
-    pdl_launch_dependents();
     if (tid == 0) {
         for (int b = 0; b < NBUF; ++b)
             mbar_init(&full[b], 1);
@@ -771,6 +778,7 @@ __global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs 
                 }
             });
     }
+    pdl_launch_dependents();  // only now (see the note above the ring kernel)
     // Every copy issued was waited for above unless a wait gave up; then make sure none is still
     // landing before the CTA leaves -- the last fill of each buffer (bounded) -- and raise the
     // fault word.
