@@ -64,7 +64,7 @@ struct ExactSlot {
 };
 
 // Barrier of the threads that share a row: the whole CTA (bar 0), or the `nt` threads of named
-// barrier `bar` (a row group of a multi-group CTA, or the ring's consumer warps).
+// barrier `bar` (the ring kernel's consumer warps).
 __device__ __forceinline__ void group_sync(int bar, int nt)
 {
     if (bar == 0)
@@ -86,7 +86,7 @@ struct Vecs {
 // code and few registers.
 template <int VPT>
 __device__ __forceinline__ float block_sum_exact(const Vecs<VPT> vv, ExactSlot *xslot, int nt,
-                                                 int wbase, int bar)
+                                                 int bar)
 {
     const uint4 (&v)[VPT] = vv.v;
     const int lane = threadIdx.x & 31;
@@ -107,7 +107,7 @@ __device__ __forceinline__ float block_sum_exact(const Vecs<VPT> vv, ExactSlot *
         xslot[warp].max_bits = mx;
     group_sync(bar, nt);
     for (int w = 0; w < nw; ++w)
-        mx = max(mx, xslot[wbase + w].max_bits);
+        mx = max(mx, xslot[w].max_bits);
     if (mx >= 0x7f800000u)  // a NaN or infinite square: the IEEE sum
         return __uint_as_float(mx > 0x7f800000u ? 0x7fc00000u : 0x7f800000u);
     if (mx == 0u)
@@ -138,7 +138,7 @@ __device__ __forceinline__ float block_sum_exact(const Vecs<VPT> vv, ExactSlot *
     group_sync(bar, nt);
     ExactAcc t = {0ull, 0ull, 0u};
     for (int w = 0; w < nw; ++w)
-        exact_merge(t, ExactAcc{xslot[wbase + w].hi, xslot[wbase + w].lo, xslot[wbase + w].sticky});
+        exact_merge(t, ExactAcc{xslot[w].hi, xslot[w].lo, xslot[w].sticky});
     return exact_round(t, emax);
 }
 
@@ -163,16 +163,15 @@ __device__ __forceinline__ Sum2 lanes_merged(const Sum2x2 &a)
     return sum_merge(Sum2{lo_of(a.hi), lo_of(a.lo)}, Sum2{hi_of(a.hi), hi_of(a.lo)});
 }
 
-// Sum over the `nt` threads of a row group (a multiple of 32; its warps are wbase, wbase + 1, ...
-// of the CTA, synchronised by group_sync(bar, nt)) of the squares of their vectors `v`, of which
-// each thread has formed the compensated partial sum `acc`; rounded as the exact sum would be.
-// Warp partials go through `slot` / `xslot` (indexed by the CTA's warp index; no concurrent
-// reduction of another group uses those entries); every warp combines them with the same
-// butterfly, so all threads get identical bits and take the rare exact path together.
+// Sum over the first `nt` threads of the CTA (a multiple of 32, synchronised by
+// group_sync(bar, nt)) of the squares of their vectors `v`, of which each thread has formed the
+// compensated partial sum `acc`; rounded as the exact sum would be.  Warp partials go through
+// `slot` / `xslot` (>= nt / 32 entries no concurrent reduction uses); every warp combines them
+// with the same butterfly, so all threads get identical bits and take the rare exact path
+// together.
 template <int VPT>
 __device__ __forceinline__ float block_sum_sq(const Sum2x2 &acc, const uint4 (&v)[VPT],
-                                              Sum2 *slot, ExactSlot *xslot, int nt, int wbase,
-                                              int bar)
+                                              Sum2 *slot, ExactSlot *xslot, int nt, int bar)
 {
     const Sum2 a = warp_sum(lanes_merged(acc));
     const int lane = threadIdx.x & 31;
@@ -180,7 +179,7 @@ __device__ __forceinline__ float block_sum_sq(const Sum2x2 &acc, const uint4 (&v
     if (lane == 0)
         slot[threadIdx.x >> 5] = a;
     group_sync(bar, nt);
-    Sum2 p = lane < nw ? slot[wbase + lane] : Sum2{0.0f, 0.0f};
+    Sum2 p = lane < nw ? slot[lane] : Sum2{0.0f, 0.0f};
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         if (off < nw) {
@@ -200,7 +199,7 @@ __device__ __forceinline__ float block_sum_sq(const Sum2x2 &acc, const uint4 (&v
 #pragma unroll
     for (int i = 0; i < VPT; ++i)
         vv.v[i] = v[i];
-    return block_sum_exact<VPT>(vv, xslot, nt, wbase, bar);
+    return block_sum_exact<VPT>(vv, xslot, nt, bar);
 }
 
 // Block-wide sum over `nt` threads of the squares of their vectors, in plain FP32 and a fixed
@@ -210,7 +209,7 @@ __device__ __forceinline__ float block_sum_sq(const Sum2x2 &acc, const uint4 (&v
 // BF16 ulp, unlike r, whose effect reaches h' through a sum that can cancel.
 template <int VPT>
 __device__ __forceinline__ float block_sum_sq_plain(const uint4 (&v)[VPT], float *slot, int nt,
-                                                    int wbase, int bar)
+                                                    int bar)
 {
     f2 s0 = 0ull, s1 = 0ull;
 #pragma unroll
@@ -232,9 +231,9 @@ __device__ __forceinline__ float block_sum_sq_plain(const uint4 (&v)[VPT], float
     if ((threadIdx.x & 31) == 0)
         slot[threadIdx.x >> 5] = t;
     group_sync(bar, nt);
-    t = slot[wbase];
+    t = slot[0];
     for (int w = 1; w < nw; ++w)
-        t = __fadd_rn(t, slot[wbase + w]);
+        t = __fadd_rn(t, slot[w]);
     return t;
 }
 
@@ -265,9 +264,9 @@ using SrcParts = typename std::conditional<SRC == kSrcTp, TpParts, NoParts>::typ
 __device__ __forceinline__ const void *part_ptr(const TpParts &x, int p) { return x.p[p]; }
 __device__ __forceinline__ const void *part_ptr(const NoParts &, int) { return nullptr; }
 
-// The boundary chain for one row whose inputs sit in registers: xv (x) and hv (h) hold the
-// vectors gtid + i * nt of thread gtid of the row's group (nt threads, warps wbase.. of the CTA,
-// barrier `bar`: see block_sum_sq).  wpo(i) / wpr(i) give the matching weight vectors.
+// The boundary chain for one row whose inputs sit in registers: xv (x) and hv (h) hold this
+// thread's vectors tid + i * nt of the row (nt threads synchronised by barrier `bar`: see
+// block_sum_sq).  wpo(i) / wpr(i) give the matching weight vectors.
 // `after_first_sum` runs right after the first block reduction.  `fail` (persistent kernels;
 // null otherwise) is the CTA's flag that a wait on its own copies ran out.  It is read right after
 // the first block reduction, whose barrier follows every thread's waits for this row (a thread
@@ -278,17 +277,17 @@ template <int VPT, typename WPost, typename WPre, typename AfterFirstSum>
 __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t row,
                                                const uint4 (&xv)[VPT], const uint4 (&hv)[VPT],
                                                WPost wpo, WPre wpr, Sum2 *red,
-                                               ExactSlot *xred, float *pred, int nt, int gtid,
-                                               int wbase, int bar, const volatile int *fail,
+                                               ExactSlot *xred, float *pred, int nt, int bar,
+                                               const volatile int *fail,
                                                AfterFirstSum after_first_sum)
 {
     const int nvec = a.H >> 3;
-    const int tid = gtid;
+    const int tid = threadIdx.x;
     const int64_t row_off = row * (int64_t)a.H;
 
     // ---- a1: r = 1/sqrt(mean(x^2) + eps) ---------------------------------------------------
-    const float r = rms_inv(block_sum_sq(squares_sum(xv), xv, red, xred, nt, wbase, bar),
-                            (float)a.H, a.eps);
+    const float r =
+        rms_inv(block_sum_sq(squares_sum(xv), xv, red, xred, nt, bar), (float)a.H, a.eps);
     const bool dead = fail != nullptr && *fail != 0;
     after_first_sum();
 
@@ -324,8 +323,7 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
             }
         }
     }
-    const f2 rr2 =
-        splat(rms_inv(block_sum_sq_plain(hp, pred, nt, wbase, bar), (float)a.H, a.eps));
+    const f2 rr2 = splat(rms_inv(block_sum_sq_plain(hp, pred, nt, bar), (float)a.H, a.eps));
     if (dead)
         return;  // a wait on this CTA's copies gave up: write nothing
 
@@ -493,7 +491,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
         }
         boundary_chain<VPT>(
             a, row, xv, hv, [&](int i) { return wpo[i]; }, [&](int i) { return wpr[i]; }, red,
-            xred, pred, nt, tid, 0, 0, nullptr, [] {});
+            xred, pred, nt, 0, nullptr, [] {});
     }
 }
 
@@ -507,7 +505,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
 // bulk copies have landed (transaction bytes), `empty` when all consumer warps have read the
 // stage (one arrive per warp).  The producer keeps `stages` units in flight.
 //
-// a.starve (the diagnostic beam_selftest_persistent_timeout) arms the `full` barriers without
+// `starve` (the diagnostic beam_selftest_persistent_timeout) arms the `full` barriers without
 // issuing the copies and reads no routing weights: the consumers' first wait runs out after
 // a.wait_ns, and the kernel writes nothing.
 
@@ -675,8 +673,8 @@ __global__ void __launch_bounds__(NC + 32, MINB)
         }
         boundary_chain<VPT>(
             a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
-            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, tid, 0, 1,
-            vfail, [] {});
+            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, 1, vfail,
+            [] {});
     }
     pdl_launch_dependents();  // only now (see the note above the ring kernel)
     if (tid == 0 && *vfail)
@@ -770,8 +768,8 @@ __global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs 
         const bool refill = i + NBUF < my_rows;
         boundary_chain<VPT>(
             a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
-            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, tid, 0, 0,
-            vfail, [&] {
+            [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, 0, vfail,
+            [&] {
                 if (tid == 0 && refill && !*vfail) {
                     issue(row + NBUF * stride, b);
                     ++refills;
