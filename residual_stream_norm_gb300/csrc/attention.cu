@@ -446,8 +446,9 @@ __device__ __forceinline__ void cp_async_wait_one() { asm volatile("cp.async.wai
 // A thread reads back only what it copied itself, so no barrier guards the staging buffers;
 // [pass parity][vector][thread] keeps a warp's reads of one vector contiguous (no bank
 // conflicts).
-// 4 CTAs of 8 warps on an SM (64 registers) without a KV cache; with one, 3 CTAs (85 registers):
-// at 64 its V path and cache stores spilled, and it took 110.6 us against 104.8 us at T = 16384.
+// 4 CTAs of 8 warps on an SM (at most 64 registers) without a KV cache; with one, 3 CTAs (at most
+// 85): at 64 its V path and cache stores spilled, and it took 110.6 us against 104.8 us at
+// T = 16384.
 template <bool ROPE, int TT, bool KV>
 __global__ void __launch_bounds__(kQkThreads, KV ? 3 : 4)
     qk_stage_kernel(const QkArgs a, const RopeTable tab)
