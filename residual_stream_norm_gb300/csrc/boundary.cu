@@ -273,7 +273,7 @@ __device__ __forceinline__ const void *part_ptr(const NoParts &, int) { return n
 // whose wait runs out raises the flag before it reaches that barrier), and then withholds this
 // row's stores and those of every later row: no output is computed from a buffer that may not
 // have filled.  Read there, the load overlaps the arithmetic of the rest of the chain.
-template <int VPT, typename WPost, typename WPre, typename AfterFirstSum>
+template <int VPT, bool EARLY_H, typename WPost, typename WPre, typename AfterFirstSum>
 __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t row,
                                                const uint4 (&xv)[VPT], const uint4 (&hv)[VPT],
                                                WPost wpo, WPre wpr, Sum2 *red,
@@ -323,12 +323,24 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
             }
         }
     }
+    // EARLY_H: h' is final, and its stores go out ahead of the second reduction, which they
+    // overlap.  At one row per kernel (decode) the kernel's last stores bound its end: 0.16 us
+    // less a boundary than storing h' with y.  The persistent kernels store it with y (0.5 us
+    // less at 16384 rows).  The row's h was read before either way (in-place use).  A CTA whose
+    // wait gave up writes nothing; the reduction's barrier stays unconditional (threads may
+    // read the flag at different times).
+    char *h_out = (char *)a.h_out + 2 * row_off;
+    if (EARLY_H && !dead) {
+#pragma unroll
+        for (int i = 0; i < VPT; ++i)
+            if (tid + i * nt < nvec)
+                st_global(h_out + 16 * (int64_t)(tid + i * nt), hp[i]);
+    }
     const f2 rr2 = splat(rms_inv(block_sum_sq_plain(hp, pred, nt, bar), (float)a.H, a.eps));
     if (dead)
-        return;  // a wait on this CTA's copies gave up: write nothing
+        return;
 
-    // ---- a3: y = bf16((h' r') w_pre); store h' and y -----------------------------------------
-    char *h_out = (char *)a.h_out + 2 * row_off;
+    // ---- a3: y = bf16((h' r') w_pre) --------------------------------------------------------
     char *y_out = (char *)a.y_out + 2 * row_off;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
@@ -339,7 +351,8 @@ __device__ __forceinline__ void boundary_chain(const BoundaryArgs &a, int64_t ro
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 word(yv, j) = narrow(mul2(mul2(widen(word(hp[i], j)), rr2), widen(word(w, j))));
-            st_global(h_out + 16 * (int64_t)v, hp[i]);
+            if (!EARLY_H)
+                st_global(h_out + 16 * (int64_t)v, hp[i]);
             st_global(y_out + 16 * (int64_t)v, yv);
         }
     }
@@ -489,7 +502,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : (VPT == 8 ? 256 : 512))
                 hv[i] = xv[i];
             }
         }
-        boundary_chain<VPT>(
+        boundary_chain<VPT, true>(
             a, row, xv, hv, [&](int i) { return wpo[i]; }, [&](int i) { return wpr[i]; }, red,
             xred, pred, nt, 0, nullptr, [] {});
     }
@@ -671,7 +684,7 @@ __global__ void __launch_bounds__(NC + 32, MINB)
                 parity ^= 1u;
             }
         }
-        boundary_chain<VPT>(
+        boundary_chain<VPT, false>(
             a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
             [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, 1, vfail,
             [] {});
@@ -766,7 +779,7 @@ __global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs 
             }
         }
         const bool refill = i + NBUF < my_rows;
-        boundary_chain<VPT>(
+        boundary_chain<VPT, false>(
             a, row, xv, hv, [&](int k) { return wsm[k * NC + tid]; },
             [&](int k) { return wsm[(VPT + k) * NC + tid]; }, red, xred, pred, NC, 0, vfail,
             [&] {
