@@ -973,7 +973,8 @@ cudaError_t launch(const BoundaryArgs &a, const SrcParts<SRC> &parts, cudaStream
     // Few rows (or very wide rows, or more than 8 slots): one CTA per row straight from memory.
     // Blocks of at most 512 threads for few rows (320 for H = 5120, two vectors a thread: a
     // decode boundary took 2.74 us in a CUDA graph, against 3.13 us with 640 threads of one
-    // vector and 3.22 us with 160 of four), 256 or 320 otherwise.
+    // vector and 3.22 us with 160 of four, before its weight loads and h' stores were moved
+    // off its critical path; 2.49 us since), 256 or 320 otherwise.
     const bool small = a.T < 2 * (int64_t)sms;
     const int max_threads = small ? 512 : (SRC == kSrcPlain ? 256 : 320);
     const int vpt = pick_vpt(nvec, max_threads);
