@@ -711,8 +711,11 @@ __global__ void __launch_bounds__(NC + 32, MINB)
 // diagnostic beam_selftest_persistent_timeout) arms the buffers' barriers without issuing the
 // copies.
 
+// Launch bound: 3 CTAs an SM, the number its shared memory allows (two row buffers and the
+// weights, 60 KB for H = 5120); bounded for 4, the compiler held the kernel to fewer registers
+// and it took 109.3 us at T = 16384, against 107.6.
 template <int VPT, int NBUF>
-__global__ void __launch_bounds__(128, 4) boundary_pf_kernel(const BoundaryArgs a, bool starve)
+__global__ void __launch_bounds__(128, 3) boundary_pf_kernel(const BoundaryArgs a, bool starve)
 {
     constexpr int NC = 128;
     extern __shared__ __align__(128) unsigned char dyn[];
