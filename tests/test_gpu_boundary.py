@@ -130,13 +130,16 @@ def test_prefill_16384_every_row(n):
     check((u16(h_out), u16(y), rstd.cpu().numpy()), want, f"prefill n={n}")
 
 
-@pytest.mark.parametrize("which", ["rows", "persistent"])
-def test_in_place_aliasing(which):
+@pytest.mark.parametrize("which,T,H", [
+    ("rows", 33, 5120), ("rows", 33, 1032), ("rows", 33, 2056), ("rows", 33, 16384),
+    ("rows", 320, 16384), ("persistent", 0, 5120)])
+def test_in_place_aliasing(which, T, H):
     # h' over h and y over x, with guard bands; "persistent" takes T = 4 SMs + 5 rows, just enough
     # for the persistent prefetch kernel, whose row buffers are refilled while earlier rows of the
-    # same buffers are written back
-    T = 33 if which == "rows" else persistent_T()
-    c = bi.boundary_case(T=T, n=6, seed=9)
+    # same buffers are written back.  The per-row kernel stores h' ahead of its second reduction;
+    # the shapes give it 2, 1 (129 and 257 vectors: ragged warps), 4 and 8 vectors a thread
+    T = T if which == "rows" else persistent_T()
+    c = bi.boundary_case(T=T, H=H, n=6, seed=9)
     H = c["x"].shape[1]
     want = oracle.boundary(u16(c["h"]), u16(c["x"]), u16(c["w_post"]), u16(c["w_pre"]), 6)
     h, x = Guarded((T, H), fill=dev(c["h"])), Guarded((T, H), fill=dev(c["x"]))
@@ -144,8 +147,8 @@ def test_in_place_aliasing(which):
     torch.cuda.synchronize()
     h.check()
     x.check()
-    assert_bf16_close(u16(h.view), want[0], what=f"in-place h' ({which})")
-    assert_bf16_close(u16(x.view), want[1], what=f"in-place y ({which})")
+    assert_bf16_close(u16(h.view), want[0], what=f"in-place h' ({which}, T={T}, H={H})")
+    assert_bf16_close(u16(x.view), want[1], what=f"in-place y ({which}, T={T}, H={H})")
 
 
 def test_guard_bands_untouched():
