@@ -398,42 +398,39 @@ def copy_ceiling(device, nbytes: int = 1 << 30, reps: int = 20) -> dict:
             "how": "torch copy_ of a 1 GiB device buffer (read + write), 20 reps, CUDA events"}
 
 
-def host_link(device, nbytes: int = 1 << 28, reps: int = 5) -> dict:
+def host_link(device, nbytes: int = 1 << 28, reps: int = 5, trials: int = 3) -> dict:
     """Pinned host <-> device copy bandwidth measured in this run: each direction alone, and both
-    at once on two streams (the link's duplex capacity): the ceiling of the end-to-end number."""
+    at once on two streams (the link's duplex capacity): the ceiling of the end-to-end number.
+    The link is shared with the machine's other GPUs, so each figure is the best of `trials`
+    timed rounds of `reps` copies, after an untimed round of the same pattern."""
     h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     d = torch.empty(nbytes, dtype=torch.uint8, device=device)
     h2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     d2 = torch.empty(nbytes, dtype=torch.uint8, device=device)
-    out = {}
-    for name, (dst, src) in (("h2d_gb_s", (d, h)), ("d2h_gb_s", (h, d))):
-        dst.copy_(src, non_blocking=True)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    cur = torch.cuda.current_stream(device)
+
+    def timed(h2d: bool, d2h: bool) -> float:
+        """GB/s of one round: `reps` copies in each enabled direction, each on its own stream."""
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(device)
         e0.record()
-        for _ in range(reps):
-            dst.copy_(src, non_blocking=True)
+        for on, st, dst, src in ((h2d, s_in, d, h), (d2h, s_out, h2, d2)):
+            if on:
+                st.wait_event(e0)
+                with torch.cuda.stream(st):
+                    for _ in range(reps):
+                        dst.copy_(src, non_blocking=True)
+                cur.wait_stream(st)
         e1.record()
         torch.cuda.synchronize(device)
-        out[name] = round(nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
-    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(device)
-    e0.record()
-    s_in.wait_event(e0)
-    s_out.wait_event(e0)
-    with torch.cuda.stream(s_in):
-        for _ in range(reps):
-            d.copy_(h, non_blocking=True)
-    with torch.cuda.stream(s_out):
-        for _ in range(reps):
-            h2.copy_(d2, non_blocking=True)
-    cur = torch.cuda.current_stream(device)
-    cur.wait_stream(s_in)
-    cur.wait_stream(s_out)
-    e1.record()
-    torch.cuda.synchronize(device)
-    out["duplex_gb_s"] = round(2 * nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+        return (int(h2d) + int(d2h)) * nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+    out = {}
+    for name, dirs in (("h2d_gb_s", (True, False)), ("d2h_gb_s", (False, True)),
+                       ("duplex_gb_s", (True, True))):
+        timed(*dirs)  # untimed round of the same pattern
+        out[name] = round(max(timed(*dirs) for _ in range(trials)), 1)
     del h, d, h2, d2
     return out
 
