@@ -1039,8 +1039,12 @@ def main(argv=None) -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     args = ap.parse_args(argv)
+    if args.steps < 1:
+        ap.error("--steps must be >= 1")
     if args.warmup < 3:
-        ap.error("--warmup must be >= 3")
+        # at least 3 untimed steps before the timed ones; the line reports the number done
+        print(f"bench.py: --warmup {args.warmup} raised to 3", file=sys.stderr)
+        args.warmup = 3
     if args.impl == "reference":
         run_reference_arm(args)
     else:
