@@ -135,8 +135,9 @@ __device__ __forceinline__ void cache_store(void *cache, int64_t e, uint4 o, int
 
 // The per-token factors of one tile: 64 cos/sin pairs per token (RoPE), or the SSMax query
 // scale, and with a KV cache the tokens' cache slots.  cos/sin are the FP32 roundings of the exact
-// values of the FP32 angle.
-template <bool ROPE, bool KV, int TT>
+// values of the FP32 angle.  LAST_WARP: the CTA's last warp alone forms the cos/sin (two a
+// thread for a one-token tile), so that the other warps can start on their heads meanwhile.
+template <bool ROPE, bool KV, int TT, bool LAST_WARP = false>
 __device__ __forceinline__ void tile_factors(const QkArgs &a, const RopeTable &tab, int64_t t0,
                                              int nt, float (&cs)[TT][kHalf],
                                              float (&sn)[TT][kHalf], float (&scale_q)[TT],
@@ -150,7 +151,9 @@ __device__ __forceinline__ void tile_factors(const QkArgs &a, const RopeTable &t
         slot[tt] = s >= 0 && s < a.num_slots ? s : -1;
     }
     if constexpr (ROPE) {
-        for (int i = tid; i < nt * kHalf; i += blockDim.x) {
+        const int first = LAST_WARP ? (int)blockDim.x - 1 - tid : tid;  // last warp: 0..31
+        const int step = LAST_WARP ? 32 : (int)blockDim.x;
+        for (int i = first; i < nt * kHalf && (!LAST_WARP || first < 32); i += step) {
             const int tt = i / kHalf, f = i - tt * kHalf;
             const float p = (float)a.pos[t0 + tt];
             const float ang = __fmul_rn(p, tab.inv_freq[f]);
@@ -175,12 +178,13 @@ __device__ __forceinline__ void tile_factors(const QkArgs &a, const RopeTable &t
 // lane's four vectors (see above), `row` the item's row in global memory (nullptr: an inactive
 // item, whose lanes still take part in every shuffle), `hd` its head (Q heads, then K, then V),
 // `tslot` its token's cache slot, `cst` / `snt` / `sq` the token's factors.  All lanes of the
-// warp call it together.
-template <bool ROPE, bool KV>
+// warp call it together.  `before_rotate` runs right before the rotation reads cos/sin (RoPE).
+template <bool ROPE, bool KV, typename BeforeRotate>
 __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], char *row, int hd,
                                         int64_t tslot, int q, unsigned qmask,
                                         const float (&wsm)[2][kHeadDim], const float *cst,
-                                        const float *snt, float sq, f2 nz)
+                                        const float *snt, float sq, f2 nz,
+                                        BeforeRotate before_rotate)
 {
     const int nqk = a.n_q + a.n_kv;
     const bool act = row != nullptr;  // uniform across each quad
@@ -284,6 +288,7 @@ __device__ __forceinline__ void qk_item(const QkArgs &a, const uint4 (&v)[4], ch
     }
     f2 out[4][4];
     if constexpr (ROPE) {
+        before_rotate();
 #pragma unroll
         for (int jj = 0; jj < 2; ++jj) {
             const int i0 = 8 * (q + 4 * jj);  // first-half element index (< 64)
@@ -360,8 +365,13 @@ __device__ __forceinline__ char *item_row(const QkArgs &a, int64_t t, int hd, in
 // Direct kernel: a CTA of 256 threads takes tiles of TT tokens, each quad kIPP items per pass,
 // all loads of a pass issued (straight from global memory) before any arithmetic; the tile's
 // factors are computed while the first loads are in flight.  The Q and K norm weights are held
-// in shared memory as FP32.
-template <bool ROPE, int TT, bool KV>
+// in shared memory as FP32.  SPLIT (RoPE without a cache, one-token tiles): the last warp forms
+// the token's cos/sin while the other warps take their heads through the norm, and the barrier
+// comes right before the rotation (Beam's 56 heads leave that warp without a head).  It pays
+// while every CTA is resident at once (at most 4 an SM): 5.73 against 6.34 us at T = 128, 5.42
+// against 5.56 at 608; with more rounds of CTAs the wider cos/sin chain of one warp costs more
+// than it hides (10.32 against 10.18 us at 1216).
+template <bool ROPE, int TT, bool KV, bool SPLIT = false>
 __global__ void __launch_bounds__(kQkThreads, 4) qk_norm_kernel(const QkArgs a, const RopeTable tab)
 {
     __shared__ __align__(16) float cs[2][TT][kHalf];  // double-buffered by tile parity
@@ -387,6 +397,7 @@ __global__ void __launch_bounds__(kQkThreads, 4) qk_norm_kernel(const QkArgs a, 
     }
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     const int64_t ntiles = (a.T + TT - 1) / TT;
+    constexpr bool kSplit = SPLIT && ROPE && !KV && TT == 1;
     int buf = 0;
     __syncthreads();
     pdl_wait();
@@ -413,17 +424,23 @@ __global__ void __launch_bounds__(kQkThreads, 4) qk_norm_kernel(const QkArgs a, 
                 for (int jj = 0; jj < 4; ++jj)
                     v[m][jj] = row[m] ? ld_plain(row[m] + 16 * (q + 4 * jj)) : zero;
             }
-            // ---- per-token factors of the tile, once, while the first loads fly -------------
+            // ---- per-token factors of the tile, once, while the first loads fly (kSplit: by
+            // the last warp, with the barrier before the rotation) ----------------------------
             if (base == 0) {
-                tile_factors<ROPE, KV, TT>(a, tab, t0, nt, cs[buf], sn[buf], scale_q[buf],
-                                           tslot[buf]);
-                __syncthreads();
+                tile_factors<ROPE, KV, TT, kSplit>(a, tab, t0, nt, cs[buf], sn[buf],
+                                                   scale_q[buf], tslot[buf]);
+                if (!kSplit)
+                    __syncthreads();
             }
 #pragma unroll
             for (int m = 0; m < kIPP; ++m)
                 qk_item<ROPE, KV>(a, v[m], row[m], head[m], KV ? tslot[buf][tok[m]] : -1, q,
                                   qmask, wsm, cs[buf][tok[m]], sn[buf][tok[m]],
-                                  ROPE ? 0.0f : scale_q[buf][tok[m]], splat(tab.neg_zero));
+                                  ROPE ? 0.0f : scale_q[buf][tok[m]], splat(tab.neg_zero),
+                                  [&] {
+                                      if (kSplit && m == 0 && base == 0)
+                                          __syncthreads();
+                                  });
         }
     }
 }
@@ -522,7 +539,7 @@ __global__ void __launch_bounds__(kQkThreads, KV ? 3 : 4)
                 v[jj] = row ? stage[p & 1][jj][tid] : zero;
             qk_item<ROPE, KV>(a, v, row, hd, KV ? tslot[buf][tt] : -1, q, qmask, wsm,
                               cs[buf][tt], sn[buf][tt], ROPE ? 0.0f : scale_q[buf][tt],
-                              splat(tab.neg_zero));
+                              splat(tab.neg_zero), [] {});
         }
     }
 }
@@ -623,9 +640,20 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
             e = launch_pdl(qk_stage_kernel<ROPE, TT, KV>, grid, block, 0, stream, a, tab);
         else
             e = launch_pdl(qk_norm_kernel<ROPE, TT, KV>, grid, block, 0, stream, a, tab);
-    } else
-        e = launch_pdl(qk_norm_kernel<ROPE, 1, KV>, dim3(grid_for(a.T)), block, 0, stream, a,
-                       tab);
+    } else {
+        // one-token tiles; RoPE without a cache splits its cos/sin off while every CTA is
+        // resident at once (at most 4 an SM)
+        bool split = false;
+        if constexpr (ROPE && !KV)
+            split = a.T <= 4 * sms;
+        if constexpr (ROPE && !KV)
+            if (split)
+                e = launch_pdl(qk_norm_kernel<ROPE, 1, KV, true>, dim3(grid_for(a.T)), block, 0,
+                               stream, a, tab);
+        if (!split)
+            e = launch_pdl(qk_norm_kernel<ROPE, 1, KV>, dim3(grid_for(a.T)), block, 0, stream,
+                           a, tab);
+    }
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
