@@ -626,10 +626,12 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
     // RoPE (each thread then forms two cos/sin pairs per tile) and 4 for SSMax.  The staged
     // kernel keeps a second pass's reads in flight; it pays off where a head costs the most
     // arithmetic (RoPE) or the V rows add reads (the KV cache), while plain SSMax is as fast
-    // without it.  Fewer tokens: one token per CTA spreads them over more SMs.  The staged
-    // kernel's 8-token tiles need many tokens to fill the GPU: RoPE took 25.4 us at T = 2048 and
-    // 31-33 us at T = 4096 with them, against 14.1 and 27.4 us with one-token tiles (and 82 us
-    // against 104 us at T = 16384), so it starts at 32 tokens per SM.
+    // without it.  Fewer tokens: small tiles spread them over more SMs.  The staged kernel's
+    // 8-token tiles need many tokens to fill the GPU: RoPE took 25.4 us at T = 2048 and 31-33 us
+    // at T = 4096 with them, against 14.1 and 27.4 us with one-token tiles (and 82 us against
+    // 104 us at T = 16384), so it starts at 32 tokens per SM (at T = 8192 it still takes 45.2
+    // against 50.6 us for two-token tiles); below that RoPE takes the direct kernel on
+    // two-token tiles, or on one-token tiles up to 4 tokens an SM.
     const bool many = a.T >= (ROPE || KV ? 32 : 4) * sms;
     constexpr int TT = ROPE ? 8 : 4;
     const dim3 block(kQkThreads);
@@ -641,18 +643,21 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
         else
             e = launch_pdl(qk_norm_kernel<ROPE, TT, KV>, grid, block, 0, stream, a, tab);
     } else {
-        // one-token tiles; RoPE without a cache splits its cos/sin off while every CTA is
-        // resident at once (at most 4 an SM)
-        bool split = false;
-        if constexpr (ROPE && !KV)
-            split = a.T <= 4 * sms;
-        if constexpr (ROPE && !KV)
-            if (split)
+        // one-token tiles.  RoPE without a cache: while every CTA is resident at once (at most
+        // 4 an SM) it splits its cos/sin off to the last warp; past that, two-token tiles (half
+        // the CTAs, two passes each, cos/sin over 128 threads): 9.17 against 10.24 us at
+        // T = 1216, 13.07 against 14.66 at 2048 (and 5.96 against 5.42 at 608, split)
+        if constexpr (ROPE && !KV) {
+            if (a.T <= 4 * sms)
                 e = launch_pdl(qk_norm_kernel<ROPE, 1, KV, true>, dim3(grid_for(a.T)), block, 0,
                                stream, a, tab);
-        if (!split)
+            else
+                e = launch_pdl(qk_norm_kernel<ROPE, 2, KV>, dim3(grid_for((a.T + 1) / 2)), block,
+                               0, stream, a, tab);
+        } else {
             e = launch_pdl(qk_norm_kernel<ROPE, 1, KV>, dim3(grid_for(a.T)), block, 0, stream,
                            a, tab);
+        }
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }
