@@ -622,17 +622,24 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
         tab.inv_freq[i] = ROPE ? a.inv_freq_host[i] : 0.0f;
     tab.neg_zero = -0.0f;
     const int64_t sms = device_sm_count();
-    // Many tokens: 4 CTAs of 8 warps on an SM, one head per quad per pass, tiles of 8 tokens for
-    // RoPE (each thread then forms two cos/sin pairs per tile) and 4 for SSMax.  The staged
-    // kernel keeps a second pass's reads in flight; it pays off where a head costs the most
-    // arithmetic (RoPE) or the V rows add reads (the KV cache), while plain SSMax is as fast
-    // without it.  Fewer tokens: small tiles spread them over more SMs.  The staged kernel's
-    // 8-token tiles need many tokens to fill the GPU: RoPE took 25.4 us at T = 2048 and 31-33 us
-    // at T = 4096 with them, against 14.1 and 27.4 us with one-token tiles (and 82 us against
-    // 104 us at T = 16384), so it starts at 32 tokens per SM (at T = 8192 it still takes 45.2
-    // against 50.6 us for two-token tiles); below that RoPE takes the direct kernel on
-    // two-token tiles, or on one-token tiles up to 4 tokens an SM.
-    const bool many = a.T >= (ROPE || KV ? 32 : 4) * sms;
+    // Tile sizes by tokens per SM, so that the CTAs come close to filling whole rounds of 4 an
+    // SM (times at T tokens, each alternative timed back to back on one GB300):
+    //  * Many tokens (RoPE and the KV-cache variants from 32 an SM, plain SSMax from 8): 4 CTAs
+    //    of 8 warps on an SM, one head per quad per pass, tiles of 8 tokens for RoPE (each
+    //    thread then forms two cos/sin pairs per tile) and 4 for SSMax.  The staged kernel keeps
+    //    a second pass's reads in flight; it pays off where a head costs the most arithmetic
+    //    (RoPE) or the V rows add reads (the KV cache), while plain SSMax is as fast without it.
+    //    Its 8-token tiles need many tokens to fill the GPU: RoPE took 25.4 us at T = 2048 and
+    //    31-33 us at 4096 with them, against 14.1 and 27.4 us on one-token tiles, and at 8192
+    //    still 45.2 against 50.6 us on two-token tiles.
+    //  * Up to 4 tokens an SM: one-token tiles.  RoPE without a cache then splits its cos/sin
+    //    off to the last warp (5.42 against 5.96 us at T = 608 on two-token tiles).
+    //  * In between: two-token tiles.  RoPE: 9.17 against 10.24 us (one-token tiles) at
+    //    T = 1216, 13.07 against 14.66 at 2048; with a KV cache 10.84 against 12.07 at 1216 and
+    //    28.73 against 31.38 at 4096; SSMax: 3.55 against 4.49 us (4-token tiles) at 608, 5.18
+    //    against 5.77 at 1216, but 9.17 against 9.00 at 2048, where its many-token kernel
+    //    starts.
+    const bool many = ROPE || KV ? a.T >= 32 * sms : a.T > 8 * sms;
     constexpr int TT = ROPE ? 8 : 4;
     const dim3 block(kQkThreads);
     cudaError_t e;
@@ -642,22 +649,16 @@ cudaError_t launch_qk(const QkArgs &a, cudaStream_t stream)
             e = launch_pdl(qk_stage_kernel<ROPE, TT, KV>, grid, block, 0, stream, a, tab);
         else
             e = launch_pdl(qk_norm_kernel<ROPE, TT, KV>, grid, block, 0, stream, a, tab);
-    } else {
-        // one-token tiles.  RoPE without a cache: while every CTA is resident at once (at most
-        // 4 an SM) it splits its cos/sin off to the last warp; past that, two-token tiles (half
-        // the CTAs, two passes each, cos/sin over 128 threads): 9.17 against 10.24 us at
-        // T = 1216, 13.07 against 14.66 at 2048 (and 5.96 against 5.42 at 608, split)
-        if constexpr (ROPE && !KV) {
-            if (a.T <= 4 * sms)
-                e = launch_pdl(qk_norm_kernel<ROPE, 1, KV, true>, dim3(grid_for(a.T)), block, 0,
-                               stream, a, tab);
-            else
-                e = launch_pdl(qk_norm_kernel<ROPE, 2, KV>, dim3(grid_for((a.T + 1) / 2)), block,
-                               0, stream, a, tab);
-        } else {
+    } else if (a.T <= 4 * sms) {
+        if constexpr (ROPE && !KV)
+            e = launch_pdl(qk_norm_kernel<ROPE, 1, KV, true>, dim3(grid_for(a.T)), block, 0,
+                           stream, a, tab);
+        else
             e = launch_pdl(qk_norm_kernel<ROPE, 1, KV>, dim3(grid_for(a.T)), block, 0, stream,
                            a, tab);
-        }
+    } else {
+        e = launch_pdl(qk_norm_kernel<ROPE, 2, KV>, dim3(grid_for((a.T + 1) / 2)), block, 0,
+                       stream, a, tab);
     }
     return e != cudaSuccess ? e : cudaGetLastError();
 }
